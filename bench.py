@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Benchmark: sparse MLA (DSA) forward + backward on one GB300.
+
+One step is one pass of the whole hot path on one batch of synthetic input:
+dsa_fwd, then the three stages of dsa_bwd.  All calls go through the C ABI.
+
+Workload: DeepSeek-V4 "flash" layout at T=8192, H=128.  Each token has a
+128-row sliding window and 512 compressed causal top-k rows (width 640,
+non-compact).  KV holds 8192 + 2048 rows of 576 (V = the first 512
+columns).  Inputs are bf16 N(0,1) values from a seeded generator.
+
+Metrics:
+  - value: fwd+bwd TFLOPS.  fwd FLOPs = 2*H*sum_t K_t*(576+512), with K_t the
+    valid gathered slots; bwd = 2.5x fwd.
+  - gathered-KV TB/s = sum_t K_t * 1152 B * 2 passes / step time.
+  - roofline: the dominant kernel (backward main) against the measured bf16
+    peak.
+
+`--impl reference` times the fp64 CPU oracle on the host cores.  Each step is
+a bounded sample of the same workload, scaled to the same unit.
+
+Launch: python bench.py [--gpus N --steps K --warmup W] (torchrun for N > 1:
+each rank runs an independent replica, "replicas only").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FWD_FLOPS_PER_SLOT_HEAD = 2 * (576 + 512)
+BWD_MAIN_FLOPS_PER_SLOT_HEAD = 2 * (576 + 512 + 576 + 576 + 512)  # S, dP, dQ, dK, dV
+ROW_BYTES = 576 * 2
+WORKLOAD = dict(name="flash_t8k", T=8192, H=128, topk=512, window=128, W=640, S_kv=8192 + 2048,
+                compact=False)
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def make_workload(device):
+    from sparse_top_attention_gb300 import workloads as WL
+    return WL.dsv4(T=WORKLOAD["T"], H=WORKLOAD["H"], topk=WORKLOAD["topk"],
+                   compact=WORKLOAD["compact"], seed=1005, name=WORKLOAD["name"],
+                   value_device=device)
+
+
+def valid_counts(w):
+    from sparse_top_attention_gb300 import workloads as WL
+    return WL.valid_slot_count_formula(w.T, WORKLOAD["topk"])
+
+
+def cpu_oracle_sample(w, budget_s: float, rng_seed: int = 0):
+    """Time the fp64 oracle (fwd + bwd) on tokens drawn from the workload
+    until `budget_s` seconds of CPU work are done.  Returns (TFLOPS, tokens,
+    seconds)."""
+    from oracle import dsa_oracle as O
+    rng = np.random.default_rng(rng_seed)
+    counts = valid_counts(w)
+    # the host copies cover only the sampled tokens
+    kv = w.kv.cpu()
+    sink = w.sink.cpu()
+    toks_done, flops, t_used = 0, 0.0, 0.0
+    while t_used < budget_s:
+        toks = sorted(rng.choice(w.T, size=4, replace=False).tolist())
+        idx = w.topk_idxs[toks].cpu()
+        q = w.q[toks].cpu()
+        dout = w.dout[toks].cpu()
+        t0 = time.perf_counter()
+        O.forward(q, kv, idx, None, sink, w.scale)
+        O.backward(q, kv, idx, None, sink, w.scale, dout)
+        t_used += time.perf_counter() - t0
+        toks_done += len(toks)
+        flops += 3.5 * FWD_FLOPS_PER_SLOT_HEAD * w.H * float(np.sum(counts[toks]))
+    return flops / t_used / 1e12, toks_done, t_used
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    """The oracle arm: fp64 numpy on the host cores, same metric and config."""
+    if rank != 0:
+        return
+    w = make_workload("cuda" if torch.cuda.is_available() else "cpu")
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        tf, n, s = cpu_oracle_sample(w, budget_s=args.ref_step_seconds, rng_seed=i)
+        if i >= args.warmup:
+            per_step.append((tf, n, s))
+    value = float(np.mean([x[0] for x in per_step]))
+    secs = float(np.mean([x[2] for x in per_step]))
+    toks = int(np.mean([x[1] for x in per_step]))
+    line = {
+        "impl": "reference", "metric": "sparse-MLA fwd+bwd TFLOPS", "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, DeepSeek-V4 flash layout)",
+        "config": {"workload": "flash_t8k: T=8192 H=128 window 128 + top-k 512 (W=640), "
+                               "S_kv=10240, D_qk=576 D_v=512, non-compact",
+                   "sample": f"{toks} random tokens per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"fp64 numpy oracle fwd+bwd of {toks} random tokens per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    from sparse_top_attention_gb300 import dsa
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    dsa.library()
+    w = make_workload(str(dev))
+    counts = valid_counts(w)
+    sum_k = float(np.sum(counts))
+    T, H, S_kv, W = w.T, w.H, w.S_kv, w.W
+    fwd_flops = FWD_FLOPS_PER_SLOT_HEAD * H * sum_k
+    step_flops = 3.5 * fwd_flops
+    bwd_main_flops = BWD_MAIN_FLOPS_PER_SLOT_HEAD * H * sum_k
+    gathered_bytes = 2 * ROW_BYTES * sum_k  # one gather list per token, fwd + bwd
+
+    out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, H, dtype=torch.float32, device=dev)
+    dq = torch.empty(T, H, 576, dtype=torch.bfloat16, device=dev)
+    dkv = torch.empty(S_kv, 576, dtype=torch.bfloat16, device=dev)
+    dsink = torch.empty(H, dtype=torch.float32, device=dev)
+    ws = torch.empty(dsa.bwd_workspace_bytes(T, H, S_kv, W), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dsa.fwd(w.q, w.kv, w.topk_idxs, None, w.sink, w.scale, out=out, lse=lse)
+        if ev is not None:
+            ev[1].record(stream)
+        dsa.bwd(w.q, w.kv, w.topk_idxs, None, w.sink, out, lse, w.dout, w.scale, dq=dq, dkv=dkv,
+                dsink=dsink, workspace=ws, entry="dsa_bwd_preprocess")
+        if ev is not None:
+            ev[2].record(stream)
+        dsa.bwd(w.q, w.kv, w.topk_idxs, None, w.sink, out, lse, w.dout, w.scale, dq=dq, dkv=dkv,
+                dsink=dsink, workspace=ws, entry="dsa_bwd_main")
+        if ev is not None:
+            ev[3].record(stream)
+        dsa.bwd(w.q, w.kv, w.topk_idxs, None, w.sink, out, lse, w.dout, w.scale, dq=dq, dkv=dkv,
+                dsink=dsink, workspace=ws, entry="dsa_bwd_finalize")
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dsa.device_status() != 0:
+        raise RuntimeError("device status not ok after warm-up")
+
+    # Kernel launches per step: fwd 1; preprocess 2 (+ memset); main 1; finalize 2.
+    launches_per_step = 1 + 2 + 1 + 2
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    pre_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    main_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    fin_ms = float(np.mean([e[3].elapsed_time(e[4]) for e in evs]))
+    assert dsa.device_status() == 0
+
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    peaks, peak_kind = read_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    main_tflops = bwd_main_flops / (main_ms * 1e-3) / 1e12
+    fwd_tflops = fwd_flops / (fwd_ms * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        traffic = json.load(open(tpath)).get("k_bwd_main")
+
+    # End to end through the public API: pinned host inputs -> device, fwd + bwd,
+    # outputs -> pinned host, every step.
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, dev, stream, step_flops, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, n, s = cpu_oracle_sample(w, budget_s=args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores(), "kind": "oracle",
+               "sample": f"fp64 numpy oracle fwd+bwd of {n} random tokens of the workload ({s:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": "sparse-MLA fwd+bwd TFLOPS", "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded bf16 N(0,1), DeepSeek-V4 flash layout)",
+            "config": {"workload": "flash_t8k: T=8192 H=128 window 128 + top-k 512 (W=640), "
+                                   "S_kv=10240, D_qk=576 D_v=512, non-compact, B=1",
+                       "valid_slots": int(sum_k), "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (q 1.2 GB, dout 1.07 GB per step)"},
+            "gathered_kv_tbps": world * gathered_bytes / (ms_step * 1e-3) / 1e12,
+            "gathered_kv_frac_of_hbm": (gathered_bytes / (ms_step * 1e-3) / 1e9) / float(peaks["hbm_gbs"]),
+            "frac_of_bf16_peak": value / world / peak,
+            "kernels_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms,
+                           "bwd_finalize": fin_ms},
+            "fwd_tflops": fwd_tflops,
+            "roofline": {"kernel": "k_bwd_main", "bound": "tensor", "achieved": main_tflops,
+                         "peak": peak, "unit": "TFLOP/s", "frac": main_tflops / peak,
+                         "traffic": traffic, "peak_kind": f"bf16 sustained ({peak_kind})",
+                         "flops_per_launch": bwd_main_flops},
+            "clocks": clk,
+            "gpu_launches": launches_per_step * args.steps,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, dev, stream, step_flops, world):
+    from sparse_top_attention_gb300 import dsa
+    host = {k: getattr(w, k).cpu().pin_memory() for k in ("q", "kv", "topk_idxs", "sink", "dout")}
+    d = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    T, H, S_kv, W = w.T, w.H, w.S_kv, w.W
+    outs = {"out": torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev),
+            "lse": torch.empty(T, H, dtype=torch.float32, device=dev),
+            "dq": torch.empty(T, H, 576, dtype=torch.bfloat16, device=dev),
+            "dkv": torch.empty(S_kv, 576, dtype=torch.bfloat16, device=dev),
+            "dsink": torch.empty(H, dtype=torch.float32, device=dev)}
+    hout = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+    ws = torch.empty(dsa.bwd_workspace_bytes(T, H, S_kv, W), dtype=torch.uint8, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+
+    def one():
+        for k in host:
+            d[k].copy_(host[k], non_blocking=True)
+        dsa.fwd(d["q"], d["kv"], d["topk_idxs"], None, d["sink"], w.scale, out=outs["out"],
+                lse=outs["lse"])
+        dsa.bwd(d["q"], d["kv"], d["topk_idxs"], None, d["sink"], outs["out"], outs["lse"],
+                d["dout"], w.scale, dq=outs["dq"], dkv=outs["dkv"], dsink=outs["dsink"],
+                workspace=ws)
+        for k in hout:
+            hout[k].copy_(outs[k], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 10))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    return {"value": world * step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms,
+            "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=6.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) sparse MLA ("DSA") attention library.
+ *
+ * The operation: token t, query head h.
+ *   The valid slots of token t are the positions j < W with
+ *     0 <= topk_idxs[t, j] < S_kv,
+ *   and also j < topk_length[t] when a length array is given.
+ *     - cuDNN frontend "DSA backward SM90: fix three top-k and
+ *       attention-sink boundary failures", Why item 2.
+ *     - cuDNN frontend "DSA bwd SM100 fix dropped dKV gradients when topk
+ *       width > total_S_kv": a column position >= S_kv is not invalid.
+ *   s_j = scale * q[t,h,:] . kv[idx_j,:]  over all 576 columns.
+ *   lse[t,h] = log sum_j exp(s_j)  (natural log; the sink is not included).
+ *   out[t,h,:] = sum_j exp(s_j) / (sum_j exp(s_j) + exp(sink[h])) * kv[idx_j, 0:512]
+ * Every head uses the same KV tensor, whose first 512 columns are V
+ * (flash-attention "[CuTe, SM100] Support 1..128 Q heads in sparse MLA via
+ * in-kernel TMA padding", Agent Notes).  The backward takes the loss
+ * sum(dout * out) and returns dq, dkv (summed over every token and head
+ * that gathered a row) and d_sink (cuDNN page above, "Not addressed" and
+ * Testing).
+ *
+ * Conventions, for every entry point:
+ *  - Tensors are dense and row-major.  Device pointers are 16-byte aligned,
+ *    else DSA_ERR_ALIGNMENT.
+ *  - The caller owns every buffer.  The library allocates nothing and keeps
+ *    no host state; the entry points are thread-safe.
+ *  - All work is queued on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and the calls return before it finishes.
+ *  - Argument and shape errors are returned before anything is launched.
+ *    A failed launch returns DSA_ERR_CUDA.
+ *  - An index that fails the validity rule is data, not an error: it is
+ *    masked.
+ *  - An empty row (no valid slot, including topk_length <= 0) gives out = 0,
+ *    lse = -FLT_MAX, dq = 0, and adds nothing to dkv.
+ *  - topk_length > W is treated as W.
+ *  - A NULL sink means no sink, i.e. sink = -inf.
+ *  - T = 0 is a no-op.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,    /* null pointer, bad size or field */
+  DSA_ERR_UNSUPPORTED = 2,    /* valid request this build does not handle */
+  DSA_ERR_ALIGNMENT = 3,      /* a device pointer is not 16-byte aligned */
+  DSA_ERR_WORKSPACE = 4,      /* workspace missing or too small */
+  DSA_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
+  DSA_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up waiting on a barrier */
+} dsa_status_t;
+
+typedef struct {
+  int32_t T;       /* query tokens, >= 0                                   */
+  int32_t H;       /* query heads, 1..128                                  */
+  int32_t S_kv;    /* KV rows, >= 1                                        */
+  int32_t W;       /* index slots per token, >= 1                         */
+  int32_t d_qk;    /* q/kv row width; must be 576                          */
+  int32_t d_v;     /* V width (leading columns of kv); must be 512         */
+  float scale;     /* softmax scale applied to q.kv (e.g. 1/sqrt(576))     */
+  uint32_t flags;  /* reserved, must be 0                                  */
+} dsa_problem_t;
+
+/*
+ * Forward.  Shapes and types (all device pointers):
+ *   q            bf16  [T, H, 576]
+ *   kv           bf16  [S_kv, 576]
+ *   topk_idxs    int32 [T, W]
+ *   topk_length  int32 [T], or NULL for the non-compact encoding
+ *                (-1 marks unused slots)
+ *   sink         fp32  [H], natural-log logits, or NULL
+ *   out          bf16  [T, H, 512]  (written)
+ *   lse          fp32  [T, H]       (written)
+ * One kernel launch.  Limits of this build: W <= 2048.
+ */
+dsa_status_t dsa_fwd(const dsa_problem_t* problem, const void* q, const void* kv,
+                     const int32_t* topk_idxs, const int32_t* topk_length, const float* sink,
+                     void* out, float* lse, void* stream);
+
+/*
+ * Bytes of device workspace that dsa_bwd needs for `problem`.  Returns 0 on
+ * an invalid problem.  The workspace holds:
+ *   - the fp32 dkv accumulator        [S_kv, 576];
+ *   - the compacted index lists       [T, W] and their counts [T];
+ *   - per-(t,h) fp32 rows: lse*log2(e), sigma(lse - sink), delta and the
+ *     d_sink terms.
+ */
+size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem);
+
+/*
+ * Backward of the loss sum(dout * out).  Inputs are as for dsa_fwd, plus:
+ *   out    bf16 [T, H, 512]  the forward output; delta = rowsum(dout * out)
+ *                            is taken from it (the FlashAttention identity,
+ *                            cuDNN page "Not addressed")
+ *   lse    fp32 [T, H]       the forward's lse
+ *   dout   bf16 [T, H, 512]
+ * Outputs, all overwritten, never accumulated:
+ *   dq     bf16 [T, H, 576]
+ *   dkv    bf16 [S_kv, 576]  rows that no valid slot names are written as 0
+ *   dsink  fp32 [H]          must be NULL exactly when sink is NULL
+ * workspace: device memory of at least dsa_bwd_workspace_bytes(problem)
+ * bytes, 256-byte aligned.  It is overwritten.
+ * The call queues, in order: a memset, slot compaction, the delta
+ * preprocess, the main kernel, the dkv cast, and the d_sink reduce.
+ */
+dsa_status_t dsa_bwd(const dsa_problem_t* problem, const void* q, const void* kv,
+                     const int32_t* topk_idxs, const int32_t* topk_length, const float* sink,
+                     const void* out, const float* lse, const void* dout, void* dq, void* dkv,
+                     float* dsink, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The three stages that dsa_bwd queues, as separate calls for callers that
+ * want to time or interleave them.  Each takes exactly dsa_bwd's arguments
+ * and checks them the same way.  They must run in this order, on one stream
+ * and with one workspace; together they equal one dsa_bwd call.
+ *   dsa_bwd_preprocess  memset of the dkv accumulator, slot compaction and
+ *                       the delta preprocess
+ *   dsa_bwd_main        the main kernel: P recompute, dS, dq, dkv
+ *                       scatter-add
+ *   dsa_bwd_finalize    dkv fp32 -> bf16 cast and the d_sink reduce
+ */
+dsa_status_t dsa_bwd_preprocess(const dsa_problem_t* problem, const void* q, const void* kv,
+                                const int32_t* topk_idxs, const int32_t* topk_length,
+                                const float* sink, const void* out, const float* lse,
+                                const void* dout, void* dq, void* dkv, float* dsink,
+                                void* workspace, size_t workspace_bytes, void* stream);
+dsa_status_t dsa_bwd_main(const dsa_problem_t* problem, const void* q, const void* kv,
+                          const int32_t* topk_idxs, const int32_t* topk_length,
+                          const float* sink, const void* out, const float* lse, const void* dout,
+                          void* dq, void* dkv, float* dsink, void* workspace,
+                          size_t workspace_bytes, void* stream);
+dsa_status_t dsa_bwd_finalize(const dsa_problem_t* problem, const void* q, const void* kv,
+                              const int32_t* topk_idxs, const int32_t* topk_length,
+                              const float* sink, const void* out, const float* lse,
+                              const void* dout, void* dq, void* dkv, float* dsink,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Slot decode and compaction: the first step of both passes, exposed so
+ * that callers can check it bit-exactly.  For each token, the valid KV rows
+ * are written to idx_out[t, 0:count) in slot order and the count to
+ * count_out[t].  idx_out[t, count:W) is left unspecified.
+ *   idx_out    int32 [T, W]  (device)
+ *   count_out  int32 [T]     (device)
+ */
+dsa_status_t dsa_topk_compact(const dsa_problem_t* problem, const int32_t* topk_idxs,
+                              const int32_t* topk_length, int32_t* idx_out, int32_t* count_out,
+                              void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error
+ * word.  Returns:
+ *   DSA_ERR_DEVICE_TIMEOUT  a kernel gave up waiting on one of its own
+ *                           barriers (outputs of that call are garbage);
+ *   DSA_ERR_CUDA            the stream reported an error;
+ *   DSA_OK                  otherwise.
+ */
+dsa_status_t dsa_device_status(void* stream);
+
+/* Static English text for a status code. */
+const char* dsa_status_string(dsa_status_t status);
+
+/* ABI version of this library (major * 100 + minor). */
+int dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

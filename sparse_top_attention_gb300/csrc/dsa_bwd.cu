@@ -1,0 +1,572 @@
+// Sparse MLA (DSA) backward for sm_103a.
+//
+// Kernels, queued in order on the caller's stream:
+//   memset      fp32 dkv accumulator <- 0
+//   k_compact   a1: valid KV rows of every token, in slot order, and counts
+//   k_bwd_pre   b1: delta = rowsum(dout * out), lse*log2(e), gate and the
+//               per-(t,h) d_sink terms (FlashAttention "dpsum" preprocess)
+//   k_bwd_main  b2-b6: per (token, 32-head group) recompute P, form dS,
+//               accumulate dQ in TMEM, scatter-add dKV rows with fp32 atomics
+//   k_dkv_cast  fp32 accumulator -> bf16 dkv
+//   k_dsink     b7: d_sink[h] = sum_t (-p_sink * delta), fixed order
+//
+// Math per (t, h) and valid slot j.  The forward's lse excludes the sink;
+// gate = sigma(lse - sink):
+//   P_j  = exp(s_j - lse) * gate
+//   dP_j = dout . V_j
+//   dS_j = P_j * (dP_j - delta)
+//   dq   = scale * sum_j dS_j KV_j
+//   dkv[idx_j] += scale * dS_j q + P_j [dout, 0]
+//   dsink = -sum_t sigma(sink - lse) * delta
+// Sources:
+//   - cuDNN frontend "DSA backward SM90: fix three top-k and attention-sink
+//     boundary failures": Summary 1-3, Why 1-3, "Not addressed" (delta from
+//     the bf16 out; P recomputed without an online softmax, live columns
+//     satisfy s - lse <= 0).
+//   - flash-attention "[CuTe, SM100] Support 1..128 Q heads in sparse MLA via
+//     in-kernel TMA padding", Agent Notes: padded heads give dS = 0, and the
+//     d_sink reduce only covers the real heads.
+//   - cuDNN frontend "DSA bwd SM100 fix dropped dKV gradients when topk
+//     width > total_S_kv": a dkv contribution is judged by the index value
+//     and the top-k bound only.
+//
+// Main kernel tiles, transposed like the forward: gathered rows are UMMA M
+// (128) and the 32 heads of the group are N.
+//   S^T  = KV_blk . Q^T                  M=128 N=32  K=576   (smem x smem)
+//   dP^T = V_blk . dO^T                  M=128 N=32  K=512
+//   dQ^T += KV_blk^T . dS'^T             5 x (M=128 N=32 K=128)
+//   dKV_blk[:, 0:512]  = dS'^T Q + P^T dO   4 x (M=128 N=128 K=32+32)
+//   dKV_blk[:, 512:576] = dS'^T Q_rope      M=128 N=64 K=32
+// where dS' = scale * dS.  P^T is staged in TMEM as the A operand of its
+// GEMM.  dS'^T sits in one shared tile that serves as the K-major B of the
+// dQ GEMM and the MN-major A of the dKV GEMM.
+#include <cmath>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+
+BwdWorkspace bwd_workspace_layout(const Problem& p) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  BwdWorkspace w{};
+  size_t off = 0;
+  const size_t TH = static_cast<size_t>(p.T) * p.H;
+  w.dkv_acc = off; off = up(off + static_cast<size_t>(p.S_kv) * kDqk * 4);
+  w.idxc = off;    off = up(off + static_cast<size_t>(p.T) * p.W * 4);
+  w.count = off;   off = up(off + static_cast<size_t>(p.T) * 4);
+  w.lse2 = off;    off = up(off + TH * 4);
+  w.gate = off;    off = up(off + TH * 4);
+  w.delta = off;   off = up(off + TH * 4);
+  w.dsink_t = off; off = up(off + TH * 4);
+  w.total = off;
+  return w;
+}
+
+namespace {
+
+__device__ unsigned int g_err_bwd;
+
+// ------------------------------------------------------------------ a1
+
+constexpr int kCompactThreads = 256;
+
+__global__ void __launch_bounds__(kCompactThreads)
+k_compact(const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
+          int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out, int W, int S_kv) {
+  __shared__ int warp_counts[kCompactThreads / 32];
+  const int t = blockIdx.x;
+  const int len = slot_len(topk_length, t, W);
+  const int n = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, S_kv,
+                              idx_out + static_cast<size_t>(t) * W, W, warp_counts, threadIdx.x,
+                              kCompactThreads);
+  if (threadIdx.x == 0) count_out[t] = n;
+}
+
+// ------------------------------------------------------------------ b1
+
+// One warp per (t, h) row: delta = sum_d dout*out over the 512 V columns.
+__global__ void __launch_bounds__(256)
+k_bwd_pre(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
+          const float* __restrict__ lse, const float* __restrict__ sink,
+          const int32_t* __restrict__ count, float* __restrict__ lse2_o,
+          float* __restrict__ gate_o, float* __restrict__ delta_o, float* __restrict__ dsink_t,
+          int T, int H) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<long long>(T) * H) return;
+  const int t = static_cast<int>(row / H), h = static_cast<int>(row - static_cast<long long>(t) * H);
+  const uint4* o4 = reinterpret_cast<const uint4*>(out + row * kDv);
+  const uint4* d4 = reinterpret_cast<const uint4*>(dout + row * kDv);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 a = o4[lane + 32 * i], b = d4[lane + 32 * i];
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 fa = __bfloat1622float2(a2[k]), fb = __bfloat1622float2(b2[k]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    const bool empty = count[t] == 0;
+    const float l = lse[row];
+    const float sk = sink != nullptr ? sink[h] : -INFINITY;
+    // An empty row has no attention term: the sink holds the whole
+    // denominator (p_sink = 1) and P is zero.
+    const float gate = empty ? 0.f : stable_sigmoid(l - sk);
+    const float p_sink = empty ? 1.f : stable_sigmoid(sk - l);
+    lse2_o[row] = empty ? 0.f : l * kLog2e;
+    gate_o[row] = gate;
+    delta_o[row] = acc;
+    dsink_t[row] = -p_sink * acc;
+  }
+}
+
+// ------------------------------------------------------------------ b2-b6
+
+constexpr int kHG = 32;                  // heads per CTA (UMMA N of S, dP, dQ)
+constexpr int kThreads = 256;
+constexpr int kProducers = 96;           // warps 5-7
+constexpr int kKVChunk = kBlk * 128;     // 16 KB
+constexpr int kHChunk = kHG * 128;       // 4 KB: 64 columns of 32 head rows
+// smem position p of the gathered block holds d-chunk x(p): p=0 rope, p=1..8 V chunks 0..7
+constexpr int kOffKV = 0;
+constexpr int kOffQ = kOffKV + kChunks * kKVChunk;  // 9 chunks, chunk x = d-chunk x
+constexpr int kOffdO = kOffQ + kChunks * kHChunk;   // 8 chunks
+constexpr int kOffdS = kOffdO + 8 * kHChunk;        // 2 sub-tiles of 64 slots
+constexpr int kOffMisc = kOffdS + 2 * kHChunk;
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColdP = 32, kColP = 64, kColdQ = 96, kColdKV = 256;
+
+struct Misc {
+  uint64_t kv_full[kChunks];
+  uint64_t kv_free[kChunks];
+  uint64_t qd_full, s_full, ds_full, dsp_free, dq_done, mma_done;
+  uint64_t dkv_full[2], dkv_empty[2];
+  float lse2[kHG], gate[kHG], delta[kHG];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffQ % 1024 == 0 && kOffdO % 1024 == 0 && kOffdS % 1024 == 0, "alignment");
+
+__device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(&g_err_bwd, 0u, 0x1FFu);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ int dchunk_of_pos(int pos) { return pos == 0 ? 8 : pos - 1; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_bwd_main(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
+           const __nv_bfloat16* __restrict__ dout, const int32_t* __restrict__ idxc,
+           const int32_t* __restrict__ count, const float* __restrict__ lse2_g,
+           const float* __restrict__ gate_g, const float* __restrict__ delta_g,
+           float* __restrict__ dkv_acc, __nv_bfloat16* __restrict__ dq, int T, int H, int W,
+           float scale, int G) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
+  const int h0 = grp * kHG;
+  const int nh = min(kHG, H - h0);
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (tid == 0) atomicCAS(&g_err_bwd, 0u, 0x2FFu);
+    return;
+  }
+  Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
+  const FailState fs{&g_err_bwd, &m.abort_flag};
+  const int Kt = count[t];
+
+  if (Kt == 0) {  // empty row: dq = 0, no dkv contribution
+    for (int v = tid; v < nh * (kDqk / 8); v += kThreads) {
+      const int h = v / (kDqk / 8), c = v - h * (kDqk / 8);
+      *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kDqk + c * 8) =
+          make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  const int nblk = (Kt + kBlk - 1) / kBlk;
+  const int32_t* rows = idxc + static_cast<size_t>(t) * W;
+
+  if (tid == 0) {
+    for (int c = 0; c < kChunks; ++c) {
+      mbar_init(smem_u32(&m.kv_full[c]), kProducers);
+      mbar_init(smem_u32(&m.kv_free[c]), 1);
+    }
+    mbar_init(smem_u32(&m.qd_full), kProducers);
+    mbar_init(smem_u32(&m.s_full), 1);
+    mbar_init(smem_u32(&m.ds_full), 128);
+    mbar_init(smem_u32(&m.dsp_free), 1);
+    mbar_init(smem_u32(&m.dq_done), 1);
+    mbar_init(smem_u32(&m.mma_done), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&m.dkv_full[i]), 1);
+      mbar_init(smem_u32(&m.dkv_empty[i]), 128);
+    }
+    m.abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (tid < kHG) {
+    const bool real = tid < nh;
+    const size_t r = static_cast<size_t>(t) * H + h0 + tid;
+    // Padded heads get gate 0, hence P = dS = 0: they add nothing anywhere.
+    m.lse2[tid] = real ? lse2_g[r] : 0.f;
+    m.gate[tid] = real ? gate_g[r] : 0.f;
+    m.delta[tid] = real ? delta_g[r] : 0.f;
+  }
+  if (warp == 4) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (warp >= 5) {
+    // ------------------------------------------------------------ producers
+    const int ptid = tid - 160, pw = warp - 5;
+    const __nv_bfloat16* qrow0 = q + (static_cast<size_t>(t) * H + h0) * kDqk;
+    const __nv_bfloat16* drow0 = dout + (static_cast<size_t>(t) * H + h0) * kDv;
+    // Q: 32 rows x 72 pieces, then dO: 32 rows x 64 pieces (16 B each).
+    for (int p = ptid; p < kHG * 72 + kHG * 64; p += kProducers) {
+      if (p < kHG * 72) {
+        const int row = p / 72, k = p - row * 72;
+        const bool ok = row < nh;
+        const void* src = ok ? static_cast<const void*>(qrow0 + static_cast<size_t>(row) * kDqk + k * 8)
+                             : static_cast<const void*>(q);
+        cp_async_16(sbase + kOffQ + (k >> 3) * kHChunk + sw128_off(row, k & 7), src, ok ? 16u : 0u);
+      } else {
+        const int pp = p - kHG * 72;
+        const int row = pp >> 6, k = pp & 63;
+        const bool ok = row < nh;
+        const void* src = ok ? static_cast<const void*>(drow0 + static_cast<size_t>(row) * kDv + k * 8)
+                             : static_cast<const void*>(dout);
+        cp_async_16(sbase + kOffdO + (k >> 3) * kHChunk + sw128_off(row, k & 7), src, ok ? 16u : 0u);
+      }
+    }
+    cp_async_arrive(smem_u32(&m.qd_full));
+    for (int b = 0; b < nblk; ++b) {
+      for (int pos = 0; pos < kChunks; ++pos) {
+        if (b > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (b - 1) & 1, fs, 1);
+        const int x = dchunk_of_pos(pos);
+        for (int g = pw; g < kBlk / 4; g += 3) {
+          const int row = g * 4 + (lane >> 3), pc = lane & 7;
+          const int slot = b * kBlk + row;
+          const bool ok = slot < Kt;
+          const int r = ok ? rows[slot] : 0;
+          cp_async_16(sbase + kOffKV + pos * kKVChunk + sw128_off(row, pc),
+                      kv + static_cast<size_t>(r) * kDqk + x * 64 + pc * 8, ok ? 16u : 0u);
+        }
+        cp_async_arrive(smem_u32(&m.kv_full[pos]));
+      }
+    }
+    cp_async_wait_all();
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ UMMA issue
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16(128, kHG, false, false);     // S^T, dP^T
+      const uint32_t idQ = idesc_bf16(128, kHG, true, false);      // dQ^T: A MN-major, B K-major
+      const uint32_t idKV = idesc_bf16(128, 128, true, true);      // dS'^T . Q (V columns)
+      const uint32_t idKVr = idesc_bf16(128, 64, true, true);      // dS'^T . Q (rope columns)
+      const uint32_t idPT = idesc_bf16(128, 128, false, true);     // P^T (TMEM) . dO
+      mbar_wait(smem_u32(&m.qd_full), 0, fs, 2);
+      for (int b = 0; b < nblk; ++b) {
+        for (int pos = 0; pos < kChunks; ++pos) {
+          mbar_wait(smem_u32(&m.kv_full[pos]), b & 1, fs, 3);
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const int x = dchunk_of_pos(pos);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = sdesc_sw128(sbase + kOffKV + pos * kKVChunk + k * 32, 16, 1024);
+            const uint64_t bq = sdesc_sw128(sbase + kOffQ + x * kHChunk + k * 32, 16, 1024);
+            umma_ss(tmem + kColS, a, bq, idS, (pos | k) != 0);
+            if (x < 8) {
+              const uint64_t bd = sdesc_sw128(sbase + kOffdO + x * kHChunk + k * 32, 16, 1024);
+              umma_ss(tmem + kColdP, a, bd, idS, (x | k) != 0);
+            }
+          }
+        }
+        umma_commit(smem_u32(&m.s_full));
+        mbar_wait(smem_u32(&m.ds_full), b & 1, fs, 4);
+        tc_fence_after();
+        // dQ^T chunks: rope first (its second 64-row atom reads V chunk 0 as
+        // filler rows that are never stored), then d rows 0..511.
+        for (int jj = 0; jj < 5; ++jj) {
+          const int j = (jj == 0) ? 4 : jj - 1;
+          const int pos0 = (j == 4) ? 0 : 1 + 2 * j;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t a =
+                sdesc_sw128(sbase + kOffKV + pos0 * kKVChunk + kk * 2048, kKVChunk, 1024);
+            const uint64_t bs =
+                sdesc_sw128(sbase + kOffdS + (kk >> 2) * kHChunk + (kk & 3) * 32, 16, 1024);
+            umma_ss(tmem + kColdQ + j * kHG, a, bs, idQ, (b | kk) != 0);
+          }
+          if (j == 4) {
+            umma_commit(smem_u32(&m.kv_free[0]));
+          } else {
+            umma_commit(smem_u32(&m.kv_free[pos0]));
+            umma_commit(smem_u32(&m.kv_free[pos0 + 1]));
+          }
+        }
+        // dKV tile for this block's 128 gathered rows, 5 column chunks.
+        for (int n = 0; n < 5; ++n) {
+          const int gidx = b * 5 + n, buf = gidx & 1, use = gidx >> 1;
+          if (use > 0) mbar_wait(smem_u32(&m.dkv_empty[buf]), (use - 1) & 1, fs, 5);
+          tc_fence_after();
+          const uint32_t d_t = tmem + kColdKV + buf * 128;
+          if (n < 4) {
+#pragma unroll
+            for (int kk = 0; kk < kHG / 16; ++kk) {
+              const uint64_t a = sdesc_sw128(sbase + kOffdS + kk * 2048, kHChunk, 1024);
+              const uint64_t bq =
+                  sdesc_sw128(sbase + kOffQ + (2 * n) * kHChunk + kk * 2048, kHChunk, 1024);
+              umma_ss(d_t, a, bq, idKV, kk != 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < kHG / 16; ++kk) {
+              const uint64_t bd =
+                  sdesc_sw128(sbase + kOffdO + (2 * n) * kHChunk + kk * 2048, kHChunk, 1024);
+              umma_ts(d_t, tmem + kColP + kk * 8, bd, idPT, 1);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kHG / 16; ++kk) {
+              const uint64_t a = sdesc_sw128(sbase + kOffdS + kk * 2048, kHChunk, 1024);
+              const uint64_t bq = sdesc_sw128(sbase + kOffQ + 8 * kHChunk + kk * 2048, kHChunk, 1024);
+              umma_ss(d_t, a, bq, idKVr, kk != 0);
+            }
+          }
+          umma_commit(smem_u32(&m.dkv_full[buf]));
+        }
+        umma_commit(smem_u32(&m.dsp_free));
+      }
+      umma_commit(smem_u32(&m.dq_done));
+      umma_commit(smem_u32(&m.mma_done));
+      mbar_wait_final(smem_u32(&m.mma_done), 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ dS / dKV drain / dQ store
+    const float sl2 = scale * kLog2e;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int b = 0; b < nblk; ++b) {
+      mbar_wait(smem_u32(&m.s_full), b & 1, fs, 6);
+      tc_fence_after();
+      uint32_t rs[32], rd[32];
+      tmem_ld32x2_sync(tmem + lane_base + kColS, rs, tmem + lane_base + kColdP, rd);
+      const int slot = b * kBlk + tid;
+      const bool valid = slot < Kt;
+      uint32_t pk[16];
+      float dsv[kHG];
+#pragma unroll
+      for (int i = 0; i < kHG / 2; ++i) {
+        float pv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * i + e;
+          // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
+          const float p = valid ? exp2f(fmaf(__uint_as_float(rs[h]), sl2, -m.lse2[h])) * m.gate[h]
+                                : 0.f;
+          pv[e] = p;
+          dsv[h] = p * (__uint_as_float(rd[h]) - m.delta[h]) * scale;
+        }
+        pk[i] = pack_bf16x2(pv[0], pv[1]);
+      }
+      if (b > 0) {
+        mbar_wait(smem_u32(&m.dsp_free), (b - 1) & 1, fs, 7);
+        tc_fence_after();
+      }
+      tmem_st16(tmem + lane_base + kColP, pk);
+      {
+        // dS'^T tile: element (head h, slot) of a 32-row, 128-byte-swizzled tile per 64 slots.
+        const uint32_t sub = sbase + kOffdS + (tid >> 6) * kHChunk;
+        const uint32_t col = tid & 63;
+#pragma unroll
+        for (int h = 0; h < kHG; ++h) {
+          const uint32_t addr = sub + h * 128 + ((((col >> 3) ^ (h & 7)) << 4) | ((col & 7) << 1));
+          const __nv_bfloat16 v = __float2bfloat16_rn(dsv[h]);
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
+                       "h"(*reinterpret_cast<const unsigned short*>(&v))
+                       : "memory");
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&m.ds_full));
+
+      // Scatter-add this block's dKV rows.
+      const int r = valid ? rows[slot] : -1;
+      float* dst_row = dkv_acc + static_cast<size_t>(r < 0 ? 0 : r) * kDqk;
+      for (int n = 0; n < 5; ++n) {
+        const int gidx = b * 5 + n, buf = gidx & 1, use = gidx >> 1;
+        mbar_wait(smem_u32(&m.dkv_full[buf]), use & 1, fs, 8);
+        tc_fence_after();
+        const int npieces = (n < 4) ? 4 : 2;
+        for (int pc = 0; pc < npieces; ++pc) {
+          uint32_t v[32];
+          tmem_ld32_sync(tmem + lane_base + kColdKV + buf * 128 + pc * 32, v);
+          if (r >= 0) {
+            float4* d4 = reinterpret_cast<float4*>(dst_row + n * 128 + pc * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              atomicAdd(d4 + i, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                            __uint_as_float(v[4 * i + 2]),
+                                            __uint_as_float(v[4 * i + 3])));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&m.dkv_empty[buf]));
+      }
+    }
+
+    // dQ^T -> dq (bf16), staged through shared memory for coalesced stores.
+    mbar_wait(smem_u32(&m.dq_done), 0, fs, 9);
+    tc_fence_after();
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV);  // [32][576]
+    for (int j = 0; j < 5; ++j) {
+      uint32_t v[32];
+      tmem_ld32_sync(tmem + lane_base + kColdQ + j * kHG, v);
+      const int d = j * 128 + tid;
+      if (d < kDqk) {
+#pragma unroll
+        for (int h = 0; h < kHG; ++h) stage[h * kDqk + d] = __float2bfloat16_rn(__uint_as_float(v[h]));
+      }
+    }
+    named_bar_sync(1, 128);
+    for (int v = tid; v < nh * (kDqk / 8); v += 128) {
+      const int h = v / (kDqk / 8), c = v - h * (kDqk / 8);
+      *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kDqk + c * 8) =
+          *reinterpret_cast<const uint4*>(stage + h * kDqk + c * 8);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ casts and reductions
+
+__global__ void __launch_bounds__(256)
+k_dkv_cast(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dkv, long long n8) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+  uint4 o;
+  o.x = pack_bf16x2(a.x, a.y);
+  o.y = pack_bf16x2(a.z, a.w);
+  o.z = pack_bf16x2(b.x, b.y);
+  o.w = pack_bf16x2(b.z, b.w);
+  reinterpret_cast<uint4*>(dkv)[i] = o;
+}
+
+// d_sink[h] = sum over t of the per-row terms, in a fixed order (deterministic).
+__global__ void __launch_bounds__(256)
+k_dsink(const float* __restrict__ dsink_t, float* __restrict__ dsink, int T, int H) {
+  __shared__ float red[256];
+  const int h = blockIdx.x;
+  float acc = 0.f;
+  for (int t = threadIdx.x; t < T; t += 256) acc += dsink_t[static_cast<size_t>(t) * H + h];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) dsink[h] = red[0];
+}
+
+}  // namespace
+
+cudaError_t launch_compact(const Problem& p, const int32_t* idx, const int32_t* len,
+                           int32_t* idx_out, int32_t* count_out, cudaStream_t s) {
+  if (p.T == 0) return cudaSuccess;
+  k_compact<<<p.T, kCompactThreads, 0, s>>>(idx, len, idx_out, count_out, p.W, p.S_kv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const int32_t* idx,
+                       const int32_t* len, const float* sink, const void* out, const float* lse,
+                       const void* dout, void* dq, void* dkv, float* dsink, void* ws,
+                       cudaStream_t s, int stages) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const BwdWorkspace L = bwd_workspace_layout(p);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* acc = reinterpret_cast<float*>(base + L.dkv_acc);
+  int32_t* idxc = reinterpret_cast<int32_t*>(base + L.idxc);
+  int32_t* count = reinterpret_cast<int32_t*>(base + L.count);
+  float* lse2 = reinterpret_cast<float*>(base + L.lse2);
+  float* gate = reinterpret_cast<float*>(base + L.gate);
+  float* delta = reinterpret_cast<float*>(base + L.delta);
+  float* dsink_t = reinterpret_cast<float*>(base + L.dsink_t);
+  const size_t acc_bytes = static_cast<size_t>(p.S_kv) * kDqk * 4;
+  cudaError_t e = cudaSuccess;
+  if (stages & kBwdPre) {
+    e = cudaMemsetAsync(acc, 0, acc_bytes, s);
+    if (e != cudaSuccess) return e;
+    if (p.T > 0) {
+      e = launch_compact(p, idx, len, idxc, count, s);
+      if (e != cudaSuccess) return e;
+      const long long rows = static_cast<long long>(p.T) * p.H;
+      k_bwd_pre<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
+          sink, count, lse2, gate, delta, dsink_t, p.T, p.H);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
+  if ((stages & kBwdMain) && p.T > 0) {
+    const int G = (p.H + kHG - 1) / kHG;
+    k_bwd_main<<<static_cast<unsigned>(static_cast<long long>(p.T) * G), kThreads, kSmemBytes, s>>>(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kv),
+        static_cast<const __nv_bfloat16*>(dout), idxc, count, lse2, gate, delta, acc,
+        static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & kBwdFinal) {
+    const long long n8 = static_cast<long long>(p.S_kv) * kDqk / 8;
+    k_dkv_cast<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
+        acc, static_cast<__nv_bfloat16*>(dkv), n8);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (dsink != nullptr) {
+      k_dsink<<<p.H, 256, 0, s>>>(dsink_t, dsink, p.T, p.H);
+      e = cudaGetLastError();
+    }
+  }
+  return e;
+}
+
+unsigned int bwd_take_error() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_bwd, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (v) cudaMemcpyToSymbol(g_err_bwd, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace dsa

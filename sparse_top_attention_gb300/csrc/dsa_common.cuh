@@ -1,0 +1,72 @@
+// Shapes, limits and the slot-validity rule shared by the CUDA kernels.
+#pragma once
+
+#include <cstdint>
+
+#include "dsa_ptx.cuh"
+
+namespace dsa {
+
+constexpr int kDqk = 576;         // q / kv row width (512 + 64)
+constexpr int kDv = 512;          // V = kv[:, :512]
+constexpr int kRowBytes = kDqk * 2;
+constexpr int kChunks = kDqk / 64;  // 64-column (128-byte) chunks of a row
+constexpr int kBlk = 128;         // gathered slots per block (UMMA M)
+constexpr int kMaxW = 2048;       // index slots per token supported by the forward
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kFltMax = 3.402823466e38f;
+
+// Validity of slot j of a token (cuDNN frontend "DSA backward SM90: fix three
+// top-k and attention-sink boundary failures", Why item 2; cuDNN frontend
+// "DSA bwd SM100 fix dropped dKV gradients when topk width > total_S_kv"):
+// the index value must lie in [0, S_kv) and the slot must lie before the
+// clamped top-k length.  The column position is never compared with S_kv.
+__device__ __forceinline__ bool slot_valid(int32_t idx, int j, int len, int S_kv) {
+  return idx >= 0 && idx < S_kv && j < len;
+}
+
+// Effective length of a token's slot list: W without a length array,
+// otherwise topk_length[t] clamped to [0, W].
+__device__ __forceinline__ int slot_len(const int32_t* topk_length, int t, int W) {
+  if (topk_length == nullptr) return W;
+  const int n = topk_length[t];
+  return n < 0 ? 0 : (n > W ? W : n);
+}
+
+// Block-wide compaction of one token's valid rows, in slot order.
+// All `nthreads` threads (a multiple of 32) must call it.  `warp_counts`
+// is shared scratch of nthreads/32 ints.  Writes up to `cap` entries to
+// `list` (shared or global) and returns the total valid count.
+__device__ __forceinline__ int compact_token(const int32_t* __restrict__ idx_row, int W, int len,
+                                             int S_kv, int32_t* list, int cap, int* warp_counts,
+                                             int tid, int nthreads) {
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int base = 0;
+  for (int j0 = 0; j0 < W; j0 += nthreads) {
+    const int j = j0 + tid;
+    int32_t v = -1;
+    bool ok = false;
+    if (j < W) {
+      v = idx_row[j];
+      ok = slot_valid(v, j, len, S_kv);
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    if (lane == 0) warp_counts[warp] = __popc(bal);
+    __syncthreads();
+    int off = base, tot = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int c = warp_counts[w];
+      if (w < warp) off += c;
+      tot += c;
+    }
+    const int pos = off + __popc(bal & lt_mask);
+    if (ok && pos < cap) list[pos] = v;
+    base += tot;
+    __syncthreads();
+  }
+  return base;
+}
+
+}  // namespace dsa

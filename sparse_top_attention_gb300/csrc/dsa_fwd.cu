@@ -1,0 +1,375 @@
+// Sparse MLA (DSA) forward for sm_103a.
+//
+// One CTA computes one token t for a group of up to 64 query heads.  The
+// token's top-k rows are gathered from the shared KV tensor, 128 rows at a
+// time ("blocks").  The contractions use 5th-gen tensor cores with fp32
+// accumulators in TMEM, in a transposed orientation: the gathered rows form
+// the UMMA M dimension (128) and the heads form N (64), so a 64-head group
+// fills a full-rate M=128 tile.
+//   S^T[slot, h]  = sum_d KV[slot, d] * Q[h, d]          (M=128, N=64, K=576)
+//   O^T[d, h]    += sum_slot V[slot, d] * P^T[slot, h]   (4 x M=128, N=64, K=128)
+// The softmax runs on S^T in registers, one thread per gathered row.  The
+// sink enters at the end, as sigma(lse - sink):
+//   out = O * sigma(lse - sink) / l.
+// Sources:
+//   - flash-attention "[CuTe, SM100] Support 1..128 Q heads in sparse MLA via
+//     in-kernel TMA padding", Agent Notes: one token and one top-k gather list
+//     per tile; padded heads are zero rows.
+//   - cuDNN frontend "DSA backward SM90: fix three top-k and attention-sink
+//     boundary failures", Summary 1-3: empty rows, padded columns masked to
+//     -inf, a sink that stays finite when it saturates.
+//
+// Warp roles (256 threads):
+//   warps 0-3  softmax and epilogue; thread i owns TMEM lane i (gathered row i)
+//   warp 4     TMEM allocation and the single UMMA-issuing thread
+//   warps 5-7  producers: Q load, then cp.async row gathers into
+//              128B-swizzled shared tiles
+// Eight warps keep two warps per SM sub-partition, so each thread may use up
+// to 255 registers.
+#include <cmath>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+__device__ unsigned int g_err_fwd;
+
+constexpr int kHG = 64;                      // heads per CTA (UMMA N)
+constexpr int kThreads = 256;
+constexpr int kProducers = 96;              // warps 5-7
+constexpr int kQChunk = kHG * 128;           // one 64-column chunk of Q: 8 KB
+constexpr int kKVChunk = kBlk * 128;         // one 64-column chunk of 128 rows: 16 KB
+constexpr int kOffKV = 0;                    // chunks 0..7 = V (d 0..511), 8 = rope (d 512..575)
+constexpr int kOffQ = kOffKV + kChunks * kKVChunk;
+constexpr int kOffList = kOffQ + kChunks * kQChunk;
+constexpr int kOffMisc = kOffList + kMaxW * 4;
+constexpr int kOffP = kOffKV + 8 * kKVChunk;  // P^T reuses the rope chunk once S is done
+
+// TMEM columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;     // S^T: 64 columns
+constexpr uint32_t kColO = 64;    // O^T: 4 chunks x 64 columns
+
+struct Misc {
+  uint64_t kv_full[kChunks];
+  uint64_t kv_free[kChunks];
+  uint64_t q_full, s_full, p_full, o_done, mma_done;
+  float red[2][4][kHG];   // per-warp column maxima, double-buffered by block parity
+  float m_used[kHG];      // running shift per head (log2 units)
+  float fac[kHG];         // rescale factor per head, then the output scale
+  int warp_counts[kThreads / 32];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Waits on a barrier that the kernel's own tensor-core work completes,
+// ignoring the abort flag but still bounded in time.
+__device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(&g_err_fwd, 0u, 0x1FFu);
+      return;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
+           const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
+           const float* __restrict__ sink, __nv_bfloat16* __restrict__ out,
+           float* __restrict__ lse, int T, int H, int S_kv, int W, float scale, int G) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
+  const int h0 = grp * kHG;
+  const int nh = min(kHG, H - h0);
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // uniform across the CTA; never expected
+    if (tid == 0) atomicCAS(&g_err_fwd, 0u, 0x2FFu);
+    return;
+  }
+  Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
+  int32_t* list = reinterpret_cast<int32_t*>(smem + kOffList);
+  const FailState fs{&g_err_fwd, &m.abort_flag};
+
+  if (tid == 0) {
+    for (int c = 0; c < kChunks; ++c) {
+      mbar_init(smem_u32(&m.kv_full[c]), kProducers);
+      mbar_init(smem_u32(&m.kv_free[c]), 1);
+    }
+    mbar_init(smem_u32(&m.q_full), kProducers);
+    mbar_init(smem_u32(&m.s_full), 1);
+    mbar_init(smem_u32(&m.p_full), 128);
+    mbar_init(smem_u32(&m.o_done), 1);
+    mbar_init(smem_u32(&m.mma_done), 1);
+    m.abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (tid < kHG) m.m_used[tid] = -INFINITY;
+
+  // a1: decode and compact the valid slots of token t (slot order).
+  const int len = slot_len(topk_length, t, W);
+  const int Kt = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, S_kv, list, kMaxW,
+                               m.warp_counts, tid, kThreads);
+
+  if (Kt == 0) {  // empty row: out = 0, lse = -FLT_MAX, no tensor-core work
+    for (int v = tid; v < nh * (kDv / 8); v += kThreads) {
+      const int h = v / (kDv / 8), c = v - h * (kDv / 8);
+      *reinterpret_cast<uint4*>(out + (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8) =
+          make_uint4(0, 0, 0, 0);
+    }
+    if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = -kFltMax;
+    return;
+  }
+  const int nblk = (Kt + kBlk - 1) / kBlk;
+
+  if (warp == 4) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (warp >= 5) {
+    // ------------------------------------------------------------ producers
+    const int ptid = tid - 160, pw = warp - 5;
+    const __nv_bfloat16* qrow0 = q + (static_cast<size_t>(t) * H + h0) * kDqk;
+    static_assert((kHG * 72) % kProducers == 0, "Q pieces split evenly");
+    for (int i = 0; i < (kHG * 72) / kProducers; ++i) {
+      const int p = ptid + kProducers * i;
+      const int row = p / 72, k = p - row * 72;
+      const bool ok = row < nh;
+      const void* src = ok ? static_cast<const void*>(qrow0 + static_cast<size_t>(row) * kDqk + k * 8)
+                           : static_cast<const void*>(q);
+      cp_async_16(sbase + kOffQ + (k >> 3) * kQChunk + sw128_off(row, k & 7), src, ok ? 16u : 0u);
+    }
+    cp_async_arrive(smem_u32(&m.q_full));
+    for (int b = 0; b < nblk; ++b) {
+      for (int c = 0; c < kChunks; ++c) {
+        if (b > 0) mbar_wait(smem_u32(&m.kv_free[c]), (b - 1) & 1, fs, 1);
+        // 32 groups of 4 rows; one warp instruction moves 4 whole 128 B row pieces.
+        for (int g = pw; g < kBlk / 4; g += 3) {
+          const int row = g * 4 + (lane >> 3), pc = lane & 7;
+          const int slot = b * kBlk + row;
+          const bool ok = slot < Kt;
+          const int r = ok ? list[slot] : 0;
+          cp_async_16(sbase + kOffKV + c * kKVChunk + sw128_off(row, pc),
+                      kv + static_cast<size_t>(r) * kDqk + c * 64 + pc * 8, ok ? 16u : 0u);
+        }
+        cp_async_arrive(smem_u32(&m.kv_full[c]));
+      }
+    }
+    cp_async_wait_all();
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ UMMA issue
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16(128, kHG, false, false);
+      const uint32_t idPV = idesc_bf16(128, kHG, true, true);
+      const uint32_t tS = tmem + kColS, tO = tmem + kColO;
+      mbar_wait(smem_u32(&m.q_full), 0, fs, 2);
+      for (int b = 0; b < nblk; ++b) {
+        for (int c = 0; c < kChunks; ++c) {
+          mbar_wait(smem_u32(&m.kv_full[c]), b & 1, fs, 3);
+          fence_proxy_async_smem();
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = sdesc_sw128(sbase + kOffKV + c * kKVChunk + k * 32, 16, 1024);
+            const uint64_t bq = sdesc_sw128(sbase + kOffQ + c * kQChunk + k * 32, 16, 1024);
+            umma_ss(tS, a, bq, idS, (c | k) != 0);
+          }
+        }
+        umma_commit(smem_u32(&m.s_full));
+        mbar_wait(smem_u32(&m.p_full), b & 1, fs, 4);
+        tc_fence_after();
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t a =
+                sdesc_sw128(sbase + kOffKV + (2 * j) * kKVChunk + k * 2048, kKVChunk, 1024);
+            const uint64_t bp = sdesc_sw128(sbase + kOffP + k * 2048, kKVChunk, 1024);
+            umma_ss(tO + j * kHG, a, bp, idPV, (b | k) != 0);
+          }
+          umma_commit(smem_u32(&m.kv_free[2 * j]));
+          umma_commit(smem_u32(&m.kv_free[2 * j + 1]));
+        }
+        umma_commit(smem_u32(&m.kv_free[8]));
+        umma_commit(smem_u32(&m.o_done));
+      }
+      umma_commit(smem_u32(&m.mma_done));
+      mbar_wait_final(smem_u32(&m.mma_done), 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const float sl2 = scale * kLog2e;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS_row = tmem + lane_base + kColS;
+    float lp[kHG];
+#pragma unroll
+    for (int h = 0; h < kHG; ++h) lp[h] = 0.f;
+    __nv_bfloat16* const sP = reinterpret_cast<__nv_bfloat16*>(smem + kOffP);
+    (void)sP;
+
+    for (int b = 0; b < nblk; ++b) {
+      mbar_wait(smem_u32(&m.s_full), b & 1, fs, 5);
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      tmem_ld32x2_sync(tS_row, r0, tS_row + 32, r1);
+      const bool valid = b * kBlk + tid < Kt;
+      float s[kHG];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        s[i] = valid ? __uint_as_float(r0[i]) * sl2 : -INFINITY;
+        s[32 + i] = valid ? __uint_as_float(r1[i]) * sl2 : -INFINITY;
+      }
+      // column (per-head) maximum over the 128 gathered rows
+      float* red = m.red[b & 1][warp];
+#pragma unroll
+      for (int h = 0; h < kHG; ++h) {
+        const float mx = warp_max(s[h]);
+        if ((h & 31) == lane) red[h] = mx;
+      }
+      named_bar_sync(1, 128);
+      bool resc = false;
+      if (tid < kHG) {
+        const float bm = fmaxf(fmaxf(m.red[b & 1][0][tid], m.red[b & 1][1][tid]),
+                               fmaxf(m.red[b & 1][2][tid], m.red[b & 1][3][tid]));
+        const float mo = m.m_used[tid];
+        const float mn = fmaxf(mo, bm);
+        // Lazy rescale: keep the old shift unless the max grew by more than
+        // 2^8; the final normalisation uses the same shift for O and l.
+        resc = mn > mo + 8.f;
+        m.fac[tid] = resc ? exp2f(mo - mn) : 1.f;
+        if (resc) m.m_used[tid] = mn;
+      }
+      const bool any = named_bar_or(1, 128, resc);
+      if (any) {
+#pragma unroll
+        for (int h = 0; h < kHG; ++h) lp[h] *= m.fac[h];
+      }
+      // P^T row as bf16 pairs; s[] is dead after this loop.
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = exp2f(s[2 * i] - m.m_used[2 * i]);
+        const float p1 = exp2f(s[2 * i + 1] - m.m_used[2 * i + 1]);
+        lp[2 * i] += p0;
+        lp[2 * i + 1] += p1;
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      if (any && b > 0) {
+        // O^T columns of heads whose shift moved: scale by 2^(old - new).
+        mbar_wait(smem_u32(&m.o_done), (b - 1) & 1, fs, 6);
+        tc_fence_after();
+        for (int j = 0; j < 4; ++j) {
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t ta = tmem + lane_base + kColO + j * kHG + half * 32;
+            uint32_t r[32];
+            tmem_ld32_sync(ta, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              r[i] = __float_as_uint(__uint_as_float(r[i]) * m.fac[half * 32 + i]);
+            tmem_st32(ta, r);
+          }
+        }
+        tmem_wait_st();
+      }
+      // Store into the swizzled MN-major tile that the PV UMMA reads.
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t dst = sbase + kOffP + sw128_off(tid, c);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
+                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&m.p_full));
+    }
+
+    // ------------------------------------------------------------ epilogue
+    mbar_wait(smem_u32(&m.o_done), (nblk - 1) & 1, fs, 7);
+    tc_fence_after();
+    float* lbuf = reinterpret_cast<float*>(smem + kOffKV);  // [128][65]
+#pragma unroll
+    for (int h = 0; h < kHG; ++h) lbuf[tid * 65 + h] = lp[h];
+    named_bar_sync(1, 128);
+    if (tid < kHG) {
+      float l = 0.f;
+      for (int r = 0; r < kBlk; ++r) l += lbuf[r * 65 + tid];
+      const float lse_nat = (m.m_used[tid] + log2f(l)) * kLn2;
+      const float sk = (sink != nullptr && tid < nh) ? sink[h0 + tid] : -INFINITY;
+      const float gate = stable_sigmoid(lse_nat - sk);
+      m.fac[tid] = gate / l;
+      if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = lse_nat;
+    }
+    named_bar_sync(1, 128);
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV + 36864);  // [64][512]
+    for (int j = 0; j < 4; ++j) {
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld32_sync(tmem + lane_base + kColO + j * kHG + half * 32, r);
+        const int d = j * 128 + tid;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int h = half * 32 + i;
+          stage[h * kDv + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * m.fac[h]);
+        }
+      }
+    }
+    named_bar_sync(1, 128);
+    for (int v = tid; v < nh * (kDv / 8); v += 128) {
+      const int h = v >> 6, c = v & 63;
+      *reinterpret_cast<uint4*>(out + (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8) =
+          *reinterpret_cast<const uint4*>(stage + h * kDv + c * 8);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const int32_t* idx,
+                       const int32_t* len, const float* sink, void* out, float* lse,
+                       cudaStream_t s) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int G = (p.H + kHG - 1) / kHG;
+  const long long grid = static_cast<long long>(p.T) * G;
+  if (grid == 0) return cudaSuccess;
+  fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kv), idx, len, sink,
+      static_cast<__nv_bfloat16*>(out), lse, p.T, p.H, p.S_kv, p.W, p.scale, G);
+  return cudaGetLastError();
+}
+
+unsigned int fwd_take_error() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_fwd, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (v) cudaMemcpyToSymbol(g_err_fwd, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace dsa

@@ -1,0 +1,47 @@
+// Launchers shared between the kernel translation units and the C-ABI layer.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace dsa {
+
+struct Problem {
+  int T, H, S_kv, W;
+  float scale;
+};
+
+// Byte offsets inside the backward workspace (256-byte aligned pieces).
+struct BwdWorkspace {
+  size_t dkv_acc;   // fp32 [S_kv, 576]
+  size_t idxc;      // int32 [T, W]   compacted rows
+  size_t count;     // int32 [T]
+  size_t lse2;      // fp32 [T, H]    lse * log2(e), 0 for empty rows
+  size_t gate;      // fp32 [T, H]    sigma(lse - sink), 0 for empty rows
+  size_t delta;     // fp32 [T, H]    rowsum(dout * out)
+  size_t dsink_t;   // fp32 [T, H]    -p_sink * delta
+  size_t total;
+};
+BwdWorkspace bwd_workspace_layout(const Problem& p);
+
+cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const int32_t* idx,
+                       const int32_t* len, const float* sink, void* out, float* lse,
+                       cudaStream_t s);
+
+cudaError_t launch_compact(const Problem& p, const int32_t* idx, const int32_t* len,
+                           int32_t* idx_out, int32_t* count_out, cudaStream_t s);
+
+// Backward stages; stage mask bit 0 = preprocess, 1 = main, 2 = finalize.
+enum : int { kBwdPre = 1, kBwdMain = 2, kBwdFinal = 4, kBwdAll = 7 };
+cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const int32_t* idx,
+                       const int32_t* len, const float* sink, const void* out, const float* lse,
+                       const void* dout, void* dq, void* dkv, float* dsink, void* ws,
+                       cudaStream_t s, int stages);
+
+// Device error words (one per translation unit): read-and-clear after a sync.
+unsigned int fwd_take_error();
+unsigned int bwd_take_error();
+
+}  // namespace dsa

@@ -1,0 +1,214 @@
+"""Python binding of the C ABI in ``include/dsa.h``: argument marshalling only.
+
+Every step of the computation runs in the CUDA library.  This module does
+three things only:
+  - checks shapes, dtypes and devices;
+  - allocates outputs and the workspace with torch when the caller passes
+    none;
+  - hands raw pointers and the current CUDA stream to the library.
+If the library has not been built, every call raises.  There is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libdsa.so")
+
+STATUS = {
+    0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_ALIGNMENT",
+    4: "DSA_ERR_WORKSPACE", 5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_TIMEOUT",
+}
+
+# Every symbol that include/dsa.h declares.
+EXPORTS = ("dsa_fwd", "dsa_bwd_workspace_bytes", "dsa_bwd", "dsa_bwd_preprocess", "dsa_bwd_main",
+           "dsa_bwd_finalize", "dsa_topk_compact", "dsa_device_status", "dsa_status_string",
+           "dsa_version")
+BWD_STAGES = ("dsa_bwd_preprocess", "dsa_bwd_main", "dsa_bwd_finalize")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("S_kv", ctypes.c_int32),
+                ("W", ctypes.c_int32), ("d_qk", ctypes.c_int32), ("d_v", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
+class DsaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({_lib_status_string(code)})")
+        self.code = code
+
+
+_lib = None
+
+
+def library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the shared library (once).  Raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing "
+                           "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+    lib = ctypes.CDLL(p)
+    vp, i32p, f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    prob = ctypes.POINTER(Problem)
+    lib.dsa_fwd.argtypes = [prob, vp, vp, i32p, i32p, f32p, vp, f32p, vp]
+    lib.dsa_fwd.restype = ctypes.c_int
+    lib.dsa_bwd_workspace_bytes.argtypes = [prob]
+    lib.dsa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    for name in ("dsa_bwd",) + BWD_STAGES:
+        fn = getattr(lib, name)
+        fn.argtypes = [prob, vp, vp, i32p, i32p, f32p, vp, f32p, vp, vp, vp, f32p, vp,
+                       ctypes.c_size_t, vp]
+        fn.restype = ctypes.c_int
+    lib.dsa_topk_compact.argtypes = [prob, i32p, i32p, i32p, i32p, vp]
+    lib.dsa_topk_compact.restype = ctypes.c_int
+    lib.dsa_device_status.argtypes = [vp]
+    lib.dsa_device_status.restype = ctypes.c_int
+    lib.dsa_status_string.argtypes = [ctypes.c_int]
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_version.argtypes = []
+    lib.dsa_version.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _lib_status_string(code: int) -> str:
+    try:
+        return library().dsa_status_string(code).decode()
+    except Exception:  # pragma: no cover - only used in error messages
+        return "?"
+
+
+def _ptr(x: Optional[torch.Tensor]):
+    return None if x is None else ctypes.c_void_p(x.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise DsaError(code, what)
+
+
+def make_problem(T, H, S_kv, W, scale) -> Problem:
+    return Problem(int(T), int(H), int(S_kv), int(W), 576, 512, float(scale), 0)
+
+
+def _need(x: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(x.shape)}, expected {tuple(shape)}")
+
+
+def _problem_from(q, kv, topk_idxs, scale):
+    T, H, dq = q.shape
+    S_kv = kv.shape[0]
+    W = topk_idxs.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dq)
+    return make_problem(T, H, S_kv, W, scale), (T, H, S_kv, W)
+
+
+def fwd(q, kv, topk_idxs, topk_length=None, sink=None, scale=None, out=None, lse=None,
+        stream=None):
+    """Sparse MLA forward.  Returns (out bf16 [T,H,512], lse fp32 [T,H])."""
+    prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale)
+    _need(q, "q", torch.bfloat16, (T, H, 576))
+    _need(kv, "kv", torch.bfloat16, (S_kv, 576))
+    _need(topk_idxs, "topk_idxs", torch.int32, (T, W))
+    if topk_length is not None:
+        _need(topk_length, "topk_length", torch.int32, (T,))
+    if sink is not None:
+        _need(sink, "sink", torch.float32, (H,))
+    if out is None:
+        out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(T, H, dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, (T, H, 512))
+    _need(lse, "lse", torch.float32, (T, H))
+    _check(library().dsa_fwd(ctypes.byref(prob), _ptr(q), _ptr(kv), _ptr(topk_idxs),
+                             _ptr(topk_length), _ptr(sink), _ptr(out), _ptr(lse), _stream(stream)),
+           "dsa_fwd")
+    return out, lse
+
+
+def bwd_workspace_bytes(T, H, S_kv, W, scale=1.0 / 24.0) -> int:
+    prob = make_problem(T, H, S_kv, W, scale)
+    return int(library().dsa_bwd_workspace_bytes(ctypes.byref(prob)))
+
+
+def bwd(q, kv, topk_idxs, topk_length, sink, out, lse, dout, scale=None, dq=None, dkv=None,
+        dsink=None, workspace=None, stream=None, entry="dsa_bwd"):
+    """Sparse MLA backward.  Returns (dq bf16, dkv bf16, dsink fp32 or None).
+
+    ``entry`` selects ``dsa_bwd`` (all stages) or one of ``BWD_STAGES``."""
+    prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale)
+    _need(q, "q", torch.bfloat16, (T, H, 576))
+    _need(kv, "kv", torch.bfloat16, (S_kv, 576))
+    _need(topk_idxs, "topk_idxs", torch.int32, (T, W))
+    if topk_length is not None:
+        _need(topk_length, "topk_length", torch.int32, (T,))
+    if sink is not None:
+        _need(sink, "sink", torch.float32, (H,))
+    _need(out, "out", torch.bfloat16, (T, H, 512))
+    _need(lse, "lse", torch.float32, (T, H))
+    _need(dout, "dout", torch.bfloat16, (T, H, 512))
+    dev = q.device
+    if dq is None:
+        dq = torch.empty(T, H, 576, dtype=torch.bfloat16, device=dev)
+    if dkv is None:
+        dkv = torch.empty(S_kv, 576, dtype=torch.bfloat16, device=dev)
+    if sink is not None and dsink is None:
+        dsink = torch.empty(H, dtype=torch.float32, device=dev)
+    nbytes = int(library().dsa_bwd_workspace_bytes(ctypes.byref(prob)))
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    if entry != "dsa_bwd" and entry not in BWD_STAGES:
+        raise ValueError(entry)
+    _check(getattr(library(), entry)(ctypes.byref(prob), _ptr(q), _ptr(kv), _ptr(topk_idxs),
+                             _ptr(topk_length), _ptr(sink), _ptr(out), _ptr(lse), _ptr(dout),
+                             _ptr(dq), _ptr(dkv), _ptr(dsink), _ptr(workspace),
+                             ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                             _stream(stream)),
+           entry)
+    return dq, dkv, dsink
+
+
+def topk_compact(topk_idxs, topk_length, S_kv, stream=None):
+    """Valid KV rows per token in slot order, and their counts (device tensors)."""
+    T, W = topk_idxs.shape
+    _need(topk_idxs, "topk_idxs", torch.int32, (T, W))
+    if topk_length is not None:
+        _need(topk_length, "topk_length", torch.int32, (T,))
+    prob = make_problem(T, 1, S_kv, W, 1.0)
+    idx_out = torch.full((T, W), -1, dtype=torch.int32, device=topk_idxs.device)
+    count = torch.empty(T, dtype=torch.int32, device=topk_idxs.device)
+    _check(library().dsa_topk_compact(ctypes.byref(prob), _ptr(topk_idxs), _ptr(topk_length),
+                                      _ptr(idx_out), _ptr(count), _stream(stream)),
+           "dsa_topk_compact")
+    return idx_out, count
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return the library's device status code."""
+    return int(library().dsa_device_status(_stream(stream)))

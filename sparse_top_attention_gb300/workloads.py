@@ -80,7 +80,7 @@ class Workload:
 
 
 def _randn_bf16(gen: torch.Generator, shape, shift: float = 0.0) -> torch.Tensor:
-    x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32, device=gen.device)
     if shift:
         x += shift
     return x.to(torch.bfloat16)
@@ -134,10 +134,16 @@ def _compact(idx: np.ndarray, S_kv: int):
     return out, length
 
 
-def dsv4(T: int, H: int, topk: int, compact: bool, seed: int, name: str) -> Workload:
-    """DeepSeek-V4-like layout: KV = T original rows + T/4 compressed rows."""
+def dsv4(T: int, H: int, topk: int, compact: bool, seed: int, name: str,
+         value_device: str = "cpu") -> Workload:
+    """DeepSeek-V4-like layout: KV = T original rows + T/4 compressed rows.
+
+    ``value_device`` chooses where q, kv, dout and sink are drawn (a seeded
+    generator on that device); indices are always drawn on the host.  The two
+    choices give different values from the same distributions.
+    """
     rng = np.random.default_rng(seed)
-    gen = torch.Generator().manual_seed(seed)
+    gen = torch.Generator(device=value_device).manual_seed(seed)
     S_kv = T + T // 4
     idx = _window_and_compressed(T, topk, rng)
     length = None
@@ -146,9 +152,10 @@ def dsv4(T: int, H: int, topk: int, compact: bool, seed: int, name: str) -> Work
     q = _randn_bf16(gen, (T, H, D_QK))
     kv = _randn_bf16(gen, (S_kv, D_QK))
     dout = _randn_bf16(gen, (T, H, D_V))
-    sink = torch.randn(H, generator=gen, dtype=torch.float32)
-    return Workload(name, q, kv, torch.from_numpy(idx.astype(np.int32)),
-                    None if length is None else torch.from_numpy(length.astype(np.int32)),
+    sink = torch.randn(H, generator=gen, dtype=torch.float32, device=gen.device)
+    dev = gen.device
+    return Workload(name, q, kv, torch.from_numpy(idx.astype(np.int32)).to(dev),
+                    None if length is None else torch.from_numpy(length.astype(np.int32)).to(dev),
                     sink, dout, 1.0 / math.sqrt(D_QK),
                     {"T": T, "H": H, "S_kv": S_kv, "W": 128 + topk, "topk": topk,
                      "compact": compact, "seed": seed})
