@@ -313,8 +313,8 @@ def run_ours(args, rank, world, local):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded bf16 N(0,1), DeepSeek-V4 flash layout)",
-            "config": {"workload": "flash_t8k: T=8192 H=128 window 128 + top-k 512 (W=640), "
-                                   "S_kv=10240, D_qk=576 D_v=512, non-compact, B=1",
+            "config": {"workload": f"{WORKLOAD['name']}: T={w.T} H=128 window 128 + top-k 512 "
+                                   f"(W=640), S_kv={w.S_kv}, D_qk=576 D_v=512, non-compact, B=1",
                        "valid_slots": int(sum_k), "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (q 1.2 GB, dout 1.07 GB per step)"},
             "gathered_kv_tbps": world * gathered_bytes / (ms_step * 1e-3) / 1e12,
@@ -390,7 +390,13 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=6.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--T", type=int, default=WORKLOAD["T"],
+                    help="tokens (smaller values only for profiling captures)")
     args = ap.parse_args()
+    if args.T != WORKLOAD["T"]:
+        WORKLOAD["T"] = args.T
+        WORKLOAD["S_kv"] = args.T + args.T // 4
+        WORKLOAD["name"] = f"flash_T{args.T}"
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -64,8 +64,24 @@ typedef struct {
   int32_t d_qk;    /* q/kv row width; must be 576                          */
   int32_t d_v;     /* V width (leading columns of kv); must be 512         */
   float scale;     /* softmax scale applied to q.kv (e.g. 1/sqrt(576))     */
-  uint32_t flags;  /* reserved, must be 0                                  */
+  uint32_t flags;  /* 0 or DSA_FLAG_DELTA_RESIDUAL                         */
 } dsa_problem_t;
+
+/*
+ * DSA_FLAG_DELTA_RESIDUAL: exact delta for the backward.
+ * By default the backward forms delta = rowsum(dout * out) from the bf16
+ * out, as the pages' kernels do.  The cuDNN page "DSA backward SM90: fix
+ * three top-k and attention-sink boundary failures" ("Not addressed")
+ * traces the remaining d_sink / dq / dkv error to that rounding and names
+ * a forward-side fix.  With this flag, `out` points to 2*T*H*512 bf16
+ * values: the rounded output [T, H, 512] followed by its rounding residual
+ * bf16(O - bf16(O)) [T, H, 512].
+ *   - dsa_fwd writes both halves.
+ *   - dsa_bwd forms delta from their sum, which carries about 16 bits of
+ *     the fp32 O.
+ * The flag must be the same in the forward and the backward call.
+ */
+#define DSA_FLAG_DELTA_RESIDUAL 1u
 
 /*
  * Forward.  Shapes and types (all device pointers):
@@ -75,7 +91,8 @@ typedef struct {
  *   topk_length  int32 [T], or NULL for the non-compact encoding
  *                (-1 marks unused slots)
  *   sink         fp32  [H], natural-log logits, or NULL
- *   out          bf16  [T, H, 512]  (written)
+ *   out          bf16  [T, H, 512]  (written; [2, T, H, 512] with
+ *                                    DSA_FLAG_DELTA_RESIDUAL)
  *   lse          fp32  [T, H]       (written)
  * One kernel launch.  Limits of this build: W <= 2048.
  */
@@ -97,7 +114,9 @@ size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem);
  * Backward of the loss sum(dout * out).  Inputs are as for dsa_fwd, plus:
  *   out    bf16 [T, H, 512]  the forward output; delta = rowsum(dout * out)
  *                            is taken from it (the FlashAttention identity,
- *                            cuDNN page "Not addressed")
+ *                            cuDNN page "Not addressed").  With
+ *                            DSA_FLAG_DELTA_RESIDUAL: [2, T, H, 512] as
+ *                            written by dsa_fwd, and delta uses hi + lo.
  *   lse    fp32 [T, H]       the forward's lse
  *   dout   bf16 [T, H, 512]
  * Outputs, all overwritten, never accumulated:

@@ -91,7 +91,7 @@ k_bwd_pre(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict
           const float* __restrict__ lse, const float* __restrict__ sink,
           const int32_t* __restrict__ count, float* __restrict__ lse2_o,
           float* __restrict__ gate_o, float* __restrict__ delta_o, float* __restrict__ dsink_t,
-          int T, int H) {
+          int T, int H, int residual) {
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<long long>(T) * H) return;
@@ -109,6 +109,21 @@ k_bwd_pre(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict
       const float2 fa = __bfloat1622float2(a2[k]), fb = __bfloat1622float2(b2[k]);
       acc = fmaf(fa.x, fb.x, acc);
       acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+  if (residual) {  // delta from out + its rounding residual (about fp32 O)
+    const uint4* l4 = reinterpret_cast<const uint4*>(out + static_cast<size_t>(T) * H * kDv + row * kDv);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 a = l4[lane + 32 * i], b = d4[lane + 32 * i];
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 fa = __bfloat1622float2(a2[k]), fb = __bfloat1622float2(b2[k]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
     }
   }
 #pragma unroll
@@ -534,7 +549,7 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
       const long long rows = static_cast<long long>(p.T) * p.H;
       k_bwd_pre<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(
           static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
-          sink, count, lse2, gate, delta, dsink_t, p.T, p.H);
+          sink, count, lse2, gate, delta, dsink_t, p.T, p.H, p.delta_residual ? 1 : 0);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }

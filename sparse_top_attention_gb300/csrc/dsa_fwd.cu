@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
            const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
            const float* __restrict__ sink, __nv_bfloat16* __restrict__ out,
-           float* __restrict__ lse, int T, int H, int S_kv, int W, float scale, int G) {
+           float* __restrict__ lse, int T, int H, int S_kv, int W, float scale, int G,
+           int residual) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
@@ -125,11 +126,13 @@ fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
   const int Kt = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, S_kv, list, kMaxW,
                                m.warp_counts, tid, kThreads);
 
+  const size_t lo_off = residual ? static_cast<size_t>(T) * H * kDv : 0;  // residual half
   if (Kt == 0) {  // empty row: out = 0, lse = -FLT_MAX, no tensor-core work
     for (int v = tid; v < nh * (kDv / 8); v += kThreads) {
       const int h = v / (kDv / 8), c = v - h * (kDv / 8);
-      *reinterpret_cast<uint4*>(out + (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8) =
-          make_uint4(0, 0, 0, 0);
+      const size_t o = (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8;
+      *reinterpret_cast<uint4*>(out + o) = make_uint4(0, 0, 0, 0);
+      if (residual) *reinterpret_cast<uint4*>(out + lo_off + o) = make_uint4(0, 0, 0, 0);
     }
     if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = -kFltMax;
     return;
@@ -317,7 +320,10 @@ fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
       if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = lse_nat;
     }
     named_bar_sync(1, 128);
-    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV + 36864);  // [64][512]
+    // Stage bf16 rows [64][512] (and their rounding residual) over the free KV
+    // tiles; the l partials there were consumed before the barrier above.
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV);
+    __nv_bfloat16* stage_lo = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV + kHG * kDv * 2);
     for (int j = 0; j < 4; ++j) {
       for (int half = 0; half < 2; ++half) {
         uint32_t r[32];
@@ -326,15 +332,21 @@ fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int h = half * 32 + i;
-          stage[h * kDv + d] = __float2bfloat16_rn(__uint_as_float(r[i]) * m.fac[h]);
+          const float o = __uint_as_float(r[i]) * m.fac[h];
+          const __nv_bfloat16 hi = __float2bfloat16_rn(o);
+          stage[h * kDv + d] = hi;
+          if (residual) stage_lo[h * kDv + d] = __float2bfloat16_rn(o - __bfloat162float(hi));
         }
       }
     }
     named_bar_sync(1, 128);
     for (int v = tid; v < nh * (kDv / 8); v += 128) {
       const int h = v >> 6, c = v & 63;
-      *reinterpret_cast<uint4*>(out + (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8) =
-          *reinterpret_cast<const uint4*>(stage + h * kDv + c * 8);
+      const size_t o = (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8;
+      *reinterpret_cast<uint4*>(out + o) = *reinterpret_cast<const uint4*>(stage + h * kDv + c * 8);
+      if (residual)
+        *reinterpret_cast<uint4*>(out + lo_off + o) =
+            *reinterpret_cast<const uint4*>(stage_lo + h * kDv + c * 8);
     }
   }
 
@@ -361,7 +373,8 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const in
   if (grid == 0) return cudaSuccess;
   fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kv), idx, len, sink,
-      static_cast<__nv_bfloat16*>(out), lse, p.T, p.H, p.S_kv, p.W, p.scale, G);
+      static_cast<__nv_bfloat16*>(out), lse, p.T, p.H, p.S_kv, p.W, p.scale, G,
+      p.delta_residual ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -11,6 +11,7 @@ namespace dsa {
 struct Problem {
   int T, H, S_kv, W;
   float scale;
+  bool delta_residual;  // out holds [2, T, H, 512]: rounded output, then its residual
 };
 
 // Byte offsets inside the backward workspace (256-byte aligned pieces).

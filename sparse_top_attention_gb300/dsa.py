@@ -31,6 +31,7 @@ EXPORTS = ("dsa_fwd", "dsa_bwd_workspace_bytes", "dsa_bwd", "dsa_bwd_preprocess"
            "dsa_bwd_finalize", "dsa_topk_compact", "dsa_device_status", "dsa_status_string",
            "dsa_version")
 BWD_STAGES = ("dsa_bwd_preprocess", "dsa_bwd_main", "dsa_bwd_finalize")
+FLAG_DELTA_RESIDUAL = 1
 
 
 class Problem(ctypes.Structure):
@@ -103,8 +104,8 @@ def _check(code: int, what: str):
         raise DsaError(code, what)
 
 
-def make_problem(T, H, S_kv, W, scale) -> Problem:
-    return Problem(int(T), int(H), int(S_kv), int(W), 576, 512, float(scale), 0)
+def make_problem(T, H, S_kv, W, scale, flags=0) -> Problem:
+    return Problem(int(T), int(H), int(S_kv), int(W), 576, 512, float(scale), int(flags))
 
 
 def _need(x: torch.Tensor, name: str, dtype, shape=None):
@@ -120,19 +121,35 @@ def _need(x: torch.Tensor, name: str, dtype, shape=None):
         raise ValueError(f"{name} has shape {tuple(x.shape)}, expected {tuple(shape)}")
 
 
-def _problem_from(q, kv, topk_idxs, scale):
+def _problem_from(q, kv, topk_idxs, scale, flags=0):
     T, H, dq = q.shape
     S_kv = kv.shape[0]
     W = topk_idxs.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(dq)
-    return make_problem(T, H, S_kv, W, scale), (T, H, S_kv, W)
+    return make_problem(T, H, S_kv, W, scale, flags), (T, H, S_kv, W)
+
+
+def _need_residual_room(out, T, H):
+    """With DSA_FLAG_DELTA_RESIDUAL the library reads/writes 2*T*H*512 bf16
+    starting at out.data_ptr(): `out` must be the first half of such a buffer."""
+    need = 2 * T * H * 512 * 2
+    st = out.untyped_storage()
+    have = st.nbytes() - (out.data_ptr() - st.data_ptr())
+    if have < need:
+        raise ValueError("delta_residual needs out to be the first half of a [2, T, H, 512] "
+                         "bf16 buffer (e.g. the `out` returned by fwd(..., delta_residual=True))")
 
 
 def fwd(q, kv, topk_idxs, topk_length=None, sink=None, scale=None, out=None, lse=None,
-        stream=None):
-    """Sparse MLA forward.  Returns (out bf16 [T,H,512], lse fp32 [T,H])."""
-    prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale)
+        stream=None, delta_residual=False):
+    """Sparse MLA forward.  Returns (out bf16 [T,H,512], lse fp32 [T,H]).
+
+    With ``delta_residual`` the output is the first half of a [2,T,H,512]
+    buffer whose second half holds the rounding residual that the backward
+    uses for an exact delta (DSA_FLAG_DELTA_RESIDUAL)."""
+    prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale,
+                                          FLAG_DELTA_RESIDUAL if delta_residual else 0)
     _need(q, "q", torch.bfloat16, (T, H, 576))
     _need(kv, "kv", torch.bfloat16, (S_kv, 576))
     _need(topk_idxs, "topk_idxs", torch.int32, (T, W))
@@ -141,7 +158,12 @@ def fwd(q, kv, topk_idxs, topk_length=None, sink=None, scale=None, out=None, lse
     if sink is not None:
         _need(sink, "sink", torch.float32, (H,))
     if out is None:
-        out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=q.device)
+        if delta_residual:
+            out = torch.empty(2, T, H, 512, dtype=torch.bfloat16, device=q.device)[0]
+        else:
+            out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=q.device)
+    if delta_residual:
+        _need_residual_room(out, T, H)
     if lse is None:
         lse = torch.empty(T, H, dtype=torch.float32, device=q.device)
     _need(out, "out", torch.bfloat16, (T, H, 512))
@@ -158,11 +180,13 @@ def bwd_workspace_bytes(T, H, S_kv, W, scale=1.0 / 24.0) -> int:
 
 
 def bwd(q, kv, topk_idxs, topk_length, sink, out, lse, dout, scale=None, dq=None, dkv=None,
-        dsink=None, workspace=None, stream=None, entry="dsa_bwd"):
+        dsink=None, workspace=None, stream=None, entry="dsa_bwd", delta_residual=False):
     """Sparse MLA backward.  Returns (dq bf16, dkv bf16, dsink fp32 or None).
 
-    ``entry`` selects ``dsa_bwd`` (all stages) or one of ``BWD_STAGES``."""
-    prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale)
+    ``entry`` selects ``dsa_bwd`` (all stages) or one of ``BWD_STAGES``.
+    ``delta_residual`` must match the forward call that produced ``out``."""
+    prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale,
+                                          FLAG_DELTA_RESIDUAL if delta_residual else 0)
     _need(q, "q", torch.bfloat16, (T, H, 576))
     _need(kv, "kv", torch.bfloat16, (S_kv, 576))
     _need(topk_idxs, "topk_idxs", torch.int32, (T, W))
@@ -173,6 +197,8 @@ def bwd(q, kv, topk_idxs, topk_length, sink, out, lse, dout, scale=None, dq=None
     _need(out, "out", torch.bfloat16, (T, H, 512))
     _need(lse, "lse", torch.float32, (T, H))
     _need(dout, "dout", torch.bfloat16, (T, H, 512))
+    if delta_residual:
+        _need_residual_room(out, T, H)
     dev = q.device
     if dq is None:
         dq = torch.empty(T, H, 576, dtype=torch.bfloat16, device=dev)

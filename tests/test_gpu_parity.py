@@ -35,12 +35,13 @@ def _lib():
     dsa.library()
 
 
-def run(w, dout=None):
+def run(w, dout=None, residual=False):
     wd = w.to(DEV)
-    out, lse = dsa.fwd(wd.q, wd.kv, wd.topk_idxs, wd.topk_length, wd.sink, wd.scale)
+    out, lse = dsa.fwd(wd.q, wd.kv, wd.topk_idxs, wd.topk_length, wd.sink, wd.scale,
+                       delta_residual=residual)
     d = wd.dout if dout is None else dout.to(DEV)
     dq, dkv, dsink = dsa.bwd(wd.q, wd.kv, wd.topk_idxs, wd.topk_length, wd.sink, out, lse, d,
-                             wd.scale)
+                             wd.scale, delta_residual=residual)
     torch.cuda.synchronize()
     assert dsa.device_status() == 0
     return out, lse, dq, dkv, dsink
@@ -49,6 +50,14 @@ def run(w, dout=None):
 def bf16_stored(x):
     """The oracle's own fp64 output, rounded to bf16 as the forward stores it."""
     return torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+
+
+def oracle_exact(w, dout=None, tokens=None):
+    """Oracle forward and backward by the definition (delta from the fp64 O)."""
+    ref = O.forward(w.q, w.kv, w.topk_idxs, w.topk_length, w.sink, w.scale, tokens=tokens)
+    g = O.backward(w.q, w.kv, w.topk_idxs, w.topk_length, w.sink, w.scale,
+                   w.dout if dout is None else dout, tokens=tokens)
+    return ref, g
 
 
 def oracle_all(w, dout=None, tokens=None):
@@ -97,11 +106,39 @@ def test_compaction_bit_exact(name, mk):
 
 # ------------------------------------------------------------------ small, every element
 
+# In the edge workloads a quarter of the (token, head) rows have q = -gamma
+# (gamma in {4, 64}) against kv with mean 1, so that some lse fall below -80.
+# The gamma = 64 rows attend one-hot.  Their dS is set by the bf16 rounding
+# of `out`, and through |q| = 64 they carry almost all of the dkv norm.
+# Under the default contract (delta from the bf16 out, as on the cuDNN page
+# "DSA backward SM90: fix three top-k and attention-sink boundary failures",
+# section "Not addressed") no implementation can reproduce that rounding
+# noise bit for bit.  So default-mode dkv on these workloads is held to
+# 2e-2.  With DSA_FLAG_DELTA_RESIDUAL (that section's forward-side fix) the
+# GPU must match the exact fp64 definition within the 1e-2 bar everywhere.
+EDGE_CONTRACT_DKV_TOL = 2e-2
+
+
 @pytest.mark.parametrize("name,mk", SMALL, ids=[s[0] for s in SMALL])
 def test_fwd_bwd_parity_small(name, mk):
+    """Default contract against the oracle whose delta uses the bf16-stored O."""
     w = mk()
     out, lse, dq, dkv, dsink = run(w)
     ref, g = oracle_all(w)
+    counts = counts_of(w)
+    ef = check_fwd(out, lse, ref, counts)
+    edge = name.startswith("edge")
+    eb = check_bwd(dq, dkv, dsink, g, counts,
+                   dkv_tol=EDGE_CONTRACT_DKV_TOL if edge else REL_TOL)
+    print(name, ef, eb)
+
+
+@pytest.mark.parametrize("name,mk", SMALL, ids=[s[0] for s in SMALL])
+def test_fwd_bwd_parity_exact_delta(name, mk):
+    """DSA_FLAG_DELTA_RESIDUAL against the exact fp64 definition."""
+    w = mk()
+    out, lse, dq, dkv, dsink = run(w, residual=True)
+    ref, g = oracle_exact(w)
     counts = counts_of(w)
     ef = check_fwd(out, lse, ref, counts)
     eb = check_bwd(dq, dkv, dsink, g, counts)
@@ -113,11 +150,15 @@ def test_fwd_bwd_parity_small(name, mk):
 def test_single_head_sink_cases(sub, compact):
     """H = 1 with each sink value, incl. +-1e38, +-2.4e38 and +-FLT_MAX."""
     w = WL.edge(H=1, compact=compact, sub=sub)
-    out, lse, dq, dkv, dsink = run(w)
-    ref, g = oracle_all(w)
+    out, lse, dq, dkv, dsink = run(w, residual=True)
+    ref, g = oracle_exact(w)
     counts = counts_of(w)
     check_fwd(out, lse, ref, counts)
     check_bwd(dq, dkv, dsink, g, counts)
+    out2, lse2, dq2, dkv2, dsink2 = run(w)
+    ref2, g2 = oracle_all(w)
+    check_fwd(out2, lse2, ref2, counts)
+    check_bwd(dq2, dkv2, dsink2, g2, counts, dkv_tol=EDGE_CONTRACT_DKV_TOL)
     sk = float(w.sink[0])
     if sk >= 1e38:  # the sink takes the whole denominator
         assert (np64(out) == 0).all() and (np64(dq) == 0).all() and (np64(dkv) == 0).all()
@@ -126,8 +167,8 @@ def test_single_head_sink_cases(sub, compact):
 @pytest.mark.parametrize("sink", [math.inf, -math.inf])
 def test_infinite_sinks(sink):
     w = WL.edge(H=24, compact=False, sink_override=sink)
-    out, lse, dq, dkv, dsink = run(w)
-    ref, g = oracle_all(w)
+    out, lse, dq, dkv, dsink = run(w, residual=True)
+    ref, g = oracle_exact(w)
     counts = counts_of(w)
     check_fwd(out, lse, ref, counts)
     check_bwd(dq, dkv, dsink, g, counts)
@@ -172,7 +213,8 @@ def test_head_padding_is_invisible():
     assert torch.equal(a[0], b[0][:, :24])   # out
     assert torch.equal(a[1], b[1][:, :24])   # lse
     assert torch.equal(a[2], b[2][:, :24])   # dq
-    assert rel_frob(a[3], b[3]) <= 1e-6      # dkv: fp32 atomics commute only up to rounding
+    # dkv: fp32 atomics land in any order, so the bf16 cast may differ by one ulp
+    assert rel_frob(a[3], b[3]) <= 1e-3
     assert torch.allclose(a[4], b[4][:24], rtol=1e-5, atol=0)
 
 
@@ -187,7 +229,7 @@ def test_repeat_launch_stress():
         dq, dkv, ds = dsa.bwd(w.q, w.kv, w.topk_idxs, w.topk_length, w.sink, out, lse, w.dout,
                               w.scale)
         assert torch.equal(out, out0) and torch.equal(lse, lse0) and torch.equal(dq, dq0)
-        assert rel_frob(dkv, dkv0) <= 1e-5
+        assert rel_frob(dkv, dkv0) <= 1e-3   # atomic order: rare one-ulp bf16 flips
     assert dsa.device_status() == 0
 
 
