@@ -191,8 +191,10 @@ def run_reference(args, rank, world):
         return
     w = make_workload("cuda" if torch.cuda.is_available() else "cpu")
     per_step = []
+    # bound the whole reference run to a few minutes whatever K and W are
+    step_s = max(0.5, min(args.ref_step_seconds, 150.0 / (args.steps + args.warmup)))
     for i in range(args.warmup + args.steps):
-        tf, n, s = cpu_oracle_sample(w, budget_s=args.ref_step_seconds, rng_seed=i)
+        tf, n, s = cpu_oracle_sample(w, budget_s=step_s, rng_seed=i)
         if i >= args.warmup:
             per_step.append((tf, n, s))
     value = float(np.mean([x[0] for x in per_step]))

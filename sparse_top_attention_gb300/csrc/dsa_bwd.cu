@@ -44,6 +44,7 @@
 
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
+#include "dsa_tmap.h"
 
 namespace dsa {
 
@@ -187,12 +188,12 @@ __device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ int dchunk_of_pos(int pos) { return pos == 0 ? 8 : pos - 1; }
 
 __global__ void __launch_bounds__(kThreads, 1)
-k_bwd_main(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
-           const __nv_bfloat16* __restrict__ dout, const int32_t* __restrict__ idxc,
+k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+           const __nv_bfloat16* __restrict__ kv, const int32_t* __restrict__ idxc,
            const int32_t* __restrict__ count, const float* __restrict__ lse2_g,
            const float* __restrict__ gate_g, const float* __restrict__ delta_g,
            float* __restrict__ dkv_acc, __nv_bfloat16* __restrict__ dq, int T, int H, int W,
-           float scale, int G) {
+           float scale, int G, int box_heads) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
@@ -223,7 +224,7 @@ k_bwd_main(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
       mbar_init(smem_u32(&m.kv_full[c]), kProducers);
       mbar_init(smem_u32(&m.kv_free[c]), 1);
     }
-    mbar_init(smem_u32(&m.qd_full), kProducers);
+    mbar_init(smem_u32(&m.qd_full), 1);
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.ds_full), 128);
     mbar_init(smem_u32(&m.dsp_free), 1);
@@ -244,6 +245,17 @@ k_bwd_main(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
     m.gate[tid] = real ? gate_g[r] : 0.f;
     m.delta[tid] = real ? delta_g[r] : 0.f;
   }
+  // Q / dO tile rows the TMA box does not cover (only when H < 32) are zero.
+  for (int i = tid; i < (kChunks + 8) * (kHG - box_heads) * 8; i += kThreads) {
+    const int per = (kHG - box_heads) * 8;
+    const int c = i / per, rem = i - c * per;
+    const int row = box_heads + rem / 8, pc = rem & 7;
+    const uint32_t base = c < kChunks ? sbase + kOffQ + c * kHChunk
+                                      : sbase + kOffdO + (c - kChunks) * kHChunk;
+    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(base + sw128_off(row, pc)), "r"(0u)
+                 : "memory");
+  }
+  fence_proxy_async_smem();
   if (warp == 4) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -251,28 +263,19 @@ k_bwd_main(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
   const uint32_t tmem = m.tmem_base;
 
   if (warp >= 5) {
-    // ------------------------------------------------------------ producers
-    const int ptid = tid - 160, pw = warp - 5;
-    const __nv_bfloat16* qrow0 = q + (static_cast<size_t>(t) * H + h0) * kDqk;
-    const __nv_bfloat16* drow0 = dout + (static_cast<size_t>(t) * H + h0) * kDv;
-    // Q: 32 rows x 72 pieces, then dO: 32 rows x 64 pieces (16 B each).
-    for (int p = ptid; p < kHG * 72 + kHG * 64; p += kProducers) {
-      if (p < kHG * 72) {
-        const int row = p / 72, k = p - row * 72;
-        const bool ok = row < nh;
-        const void* src = ok ? static_cast<const void*>(qrow0 + static_cast<size_t>(row) * kDqk + k * 8)
-                             : static_cast<const void*>(q);
-        cp_async_16(sbase + kOffQ + (k >> 3) * kHChunk + sw128_off(row, k & 7), src, ok ? 16u : 0u);
-      } else {
-        const int pp = p - kHG * 72;
-        const int row = pp >> 6, k = pp & 63;
-        const bool ok = row < nh;
-        const void* src = ok ? static_cast<const void*>(drow0 + static_cast<size_t>(row) * kDv + k * 8)
-                             : static_cast<const void*>(dout);
-        cp_async_16(sbase + kOffdO + (k >> 3) * kHChunk + sw128_off(row, k & 7), src, ok ? 16u : 0u);
-      }
+    // ------------------------------------------------------------ loads
+    // Q and dO tiles of the head group by TMA (K-major 64-column chunks of
+    // the head rows; heads past H inside the box are zero-filled), then the
+    // KV row gather with cp.async (one warp instruction = 4 whole 128 B row
+    // pieces) into the 128B-swizzled chunk tiles.
+    const int pw = warp - 5;
+    if (tid == 160) {
+      mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kChunks + 8) * box_heads * 128);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_3d(sbase + kOffQ + c * kHChunk, &tm_q, c * 64, h0, t, smem_u32(&m.qd_full));
+      for (int c = 0; c < 8; ++c)
+        tma_load_3d(sbase + kOffdO + c * kHChunk, &tm_do, c * 64, h0, t, smem_u32(&m.qd_full));
     }
-    cp_async_arrive(smem_u32(&m.qd_full));
     for (int b = 0; b < nblk; ++b) {
       for (int pos = 0; pos < kChunks; ++pos) {
         if (b > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (b - 1) & 1, fs, 1);
@@ -301,7 +304,7 @@ k_bwd_main(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
       for (int b = 0; b < nblk; ++b) {
         for (int pos = 0; pos < kChunks; ++pos) {
           mbar_wait(smem_u32(&m.kv_full[pos]), b & 1, fs, 3);
-          fence_proxy_async_smem();
+          fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
           tc_fence_after();
           const int x = dchunk_of_pos(pos);
 #pragma unroll
@@ -463,11 +466,12 @@ k_bwd_main(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
         for (int h = 0; h < kHG; ++h) stage[h * kDqk + d] = __float2bfloat16_rn(__uint_as_float(v[h]));
       }
     }
+    fence_proxy_async_smem();
     named_bar_sync(1, 128);
-    for (int v = tid; v < nh * (kDqk / 8); v += 128) {
-      const int h = v / (kDqk / 8), c = v - h * (kDqk / 8);
-      *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kDqk + c * 8) =
-          *reinterpret_cast<const uint4*>(stage + h * kDqk + c * 8);
+    if (tid == 0) {  // dq rows (t, h0..h0+nh) are contiguous
+      bulk_store(dq + (static_cast<size_t>(t) * H + h0) * kDqk, smem_u32(stage), nh * kDqk * 2);
+      bulk_commit();
+      bulk_wait_read();
     }
   }
 
@@ -556,10 +560,14 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
   }
   if ((stages & kBwdMain) && p.T > 0) {
     const int G = (p.H + kHG - 1) / kHG;
+    CUtensorMap tm_q, tm_do;
+    const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
+    e = make_head_tile_map(&tm_q, q, p.T, p.H, kDqk, box_heads);
+    if (e == cudaSuccess) e = make_head_tile_map(&tm_do, dout, p.T, p.H, kDv, box_heads);
+    if (e != cudaSuccess) return e;
     k_bwd_main<<<static_cast<unsigned>(static_cast<long long>(p.T) * G), kThreads, kSmemBytes, s>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kv),
-        static_cast<const __nv_bfloat16*>(dout), idxc, count, lse2, gate, delta, acc,
-        static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G);
+        tm_q, tm_do, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2, gate, delta, acc,
+        static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, box_heads);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -22,7 +22,8 @@
 // Warp roles (256 threads):
 //   warps 0-3  softmax and epilogue; thread i owns TMEM lane i (gathered row i)
 //   warp 4     TMEM allocation and the single UMMA-issuing thread
-//   warps 5-7  producers: Q load, then cp.async row gathers into
+//   warps 5-7  lane 0 of warp 5 issues the Q tile TMA (3-D tensor map);
+//              then the three warps gather KV rows with cp.async into
 //              128B-swizzled shared tiles
 // Eight warps keep two warps per SM sub-partition, so each thread may use up
 // to 255 registers.
@@ -30,6 +31,7 @@
 
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
+#include "dsa_tmap.h"
 
 namespace dsa {
 namespace {
@@ -38,6 +40,7 @@ __device__ unsigned int g_err_fwd;
 
 constexpr int kHG = 64;                      // heads per CTA (UMMA N)
 constexpr int kThreads = 256;
+constexpr int kQIssuer = 160;               // lane 0 of warp 5
 constexpr int kProducers = 96;              // warps 5-7
 constexpr int kQChunk = kHG * 128;           // one 64-column chunk of Q: 8 KB
 constexpr int kKVChunk = kBlk * 128;         // one 64-column chunk of 128 rows: 16 KB
@@ -87,11 +90,10 @@ __device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
-           const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
+fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
            const float* __restrict__ sink, __nv_bfloat16* __restrict__ out,
-           float* __restrict__ lse, int T, int H, int S_kv, int W, float scale, int G,
-           int residual) {
+           float* __restrict__ lse, const __nv_bfloat16* __restrict__ kv, int T, int H, int S_kv,
+           int W, float scale, int G, int residual, int box_heads) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
@@ -111,7 +113,7 @@ fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
       mbar_init(smem_u32(&m.kv_full[c]), kProducers);
       mbar_init(smem_u32(&m.kv_free[c]), 1);
     }
-    mbar_init(smem_u32(&m.q_full), kProducers);
+    mbar_init(smem_u32(&m.q_full), 1);
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.p_full), 128);
     mbar_init(smem_u32(&m.o_done), 1);
@@ -120,6 +122,26 @@ fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
     mbar_init_fence();
   }
   if (tid < kHG) m.m_used[tid] = -INFINITY;
+  // Q tile rows that the TMA box does not cover (only when H < 64) are zero.
+  for (int i = tid; i < kChunks * (kHG - box_heads) * 8; i += kThreads) {
+    const int per = (kHG - box_heads) * 8;
+    const int c = i / per, rem = i - c * per;
+    const int row = box_heads + rem / 8, pc = rem & 7;
+    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sbase + kOffQ + c * kQChunk +
+                                                               sw128_off(row, pc)),
+                 "r"(0u)
+                 : "memory");
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  // The Q tile of the head group (9 chunks of [box_heads x 64 columns], 128B
+  // swizzle; heads past H inside the box are zero-filled by the TMA) loads
+  // while the slots are decoded.
+  if (tid == kQIssuer) {
+    mbar_arrive_expect_tx(smem_u32(&m.q_full), kChunks * box_heads * 128);
+    for (int c = 0; c < kChunks; ++c)
+      tma_load_3d(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t, smem_u32(&m.q_full));
+  }
 
   // a1: decode and compact the valid slots of token t (slot order).
   const int len = slot_len(topk_length, t, W);
@@ -135,6 +157,8 @@ fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
       if (residual) *reinterpret_cast<uint4*>(out + lo_off + o) = make_uint4(0, 0, 0, 0);
     }
     if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = -kFltMax;
+    // the Q tile is still landing in this CTA's shared memory: let it finish
+    if (tid == kQIssuer) mbar_wait_final(smem_u32(&m.q_full), 0);
     return;
   }
   const int nblk = (Kt + kBlk - 1) / kBlk;
@@ -146,23 +170,14 @@ fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
   const uint32_t tmem = m.tmem_base;
 
   if (warp >= 5) {
-    // ------------------------------------------------------------ producers
-    const int ptid = tid - 160, pw = warp - 5;
-    const __nv_bfloat16* qrow0 = q + (static_cast<size_t>(t) * H + h0) * kDqk;
-    static_assert((kHG * 72) % kProducers == 0, "Q pieces split evenly");
-    for (int i = 0; i < (kHG * 72) / kProducers; ++i) {
-      const int p = ptid + kProducers * i;
-      const int row = p / 72, k = p - row * 72;
-      const bool ok = row < nh;
-      const void* src = ok ? static_cast<const void*>(qrow0 + static_cast<size_t>(row) * kDqk + k * 8)
-                           : static_cast<const void*>(q);
-      cp_async_16(sbase + kOffQ + (k >> 3) * kQChunk + sw128_off(row, k & 7), src, ok ? 16u : 0u);
-    }
-    cp_async_arrive(smem_u32(&m.q_full));
+    // ------------------------------------------------------------ gather
+    // cp.async 16-byte pieces into the 128B-swizzled chunk tiles; one warp
+    // instruction moves 4 whole 128-byte row pieces.  Rows past the valid
+    // count are zero-filled (their scores are masked).
+    const int pw = warp - 5;
     for (int b = 0; b < nblk; ++b) {
       for (int c = 0; c < kChunks; ++c) {
         if (b > 0) mbar_wait(smem_u32(&m.kv_free[c]), (b - 1) & 1, fs, 1);
-        // 32 groups of 4 rows; one warp instruction moves 4 whole 128 B row pieces.
         for (int g = pw; g < kBlk / 4; g += 3) {
           const int row = g * 4 + (lane >> 3), pc = lane & 7;
           const int slot = b * kBlk + row;
@@ -185,7 +200,7 @@ fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
       for (int b = 0; b < nblk; ++b) {
         for (int c = 0; c < kChunks; ++c) {
           mbar_wait(smem_u32(&m.kv_full[c]), b & 1, fs, 3);
-          fence_proxy_async_smem();
+          fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -339,14 +354,15 @@ fwd_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict_
         }
       }
     }
+    fence_proxy_async_smem();
     named_bar_sync(1, 128);
-    for (int v = tid; v < nh * (kDv / 8); v += 128) {
-      const int h = v >> 6, c = v & 63;
-      const size_t o = (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8;
-      *reinterpret_cast<uint4*>(out + o) = *reinterpret_cast<const uint4*>(stage + h * kDv + c * 8);
-      if (residual)
-        *reinterpret_cast<uint4*>(out + lo_off + o) =
-            *reinterpret_cast<const uint4*>(stage_lo + h * kDv + c * 8);
+    if (tid == 0) {
+      // out rows (t, h0..h0+nh) are contiguous: one bulk store per half
+      const size_t o = (static_cast<size_t>(t) * H + h0) * kDv;
+      bulk_store(out + o, smem_u32(stage), nh * kDv * 2);
+      if (residual) bulk_store(out + lo_off + o, smem_u32(stage_lo), nh * kDv * 2);
+      bulk_commit();
+      bulk_wait_read();
     }
   }
 
@@ -371,10 +387,14 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const in
   const int G = (p.H + kHG - 1) / kHG;
   const long long grid = static_cast<long long>(p.T) * G;
   if (grid == 0) return cudaSuccess;
+  CUtensorMap tm_q;
+  const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
+  cudaError_t e = make_head_tile_map(&tm_q, q, p.T, p.H, kDqk, box_heads);
+  if (e != cudaSuccess) return e;
   fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(kv), idx, len, sink,
-      static_cast<__nv_bfloat16*>(out), lse, p.T, p.H, p.S_kv, p.W, p.scale, G,
-      p.delta_residual ? 1 : 0);
+      tm_q, idx, len, sink, static_cast<__nv_bfloat16*>(out), lse,
+      static_cast<const __nv_bfloat16*>(kv), p.T, p.H, p.S_kv, p.W, p.scale, G,
+      p.delta_residual ? 1 : 0, box_heads);
   return cudaGetLastError();
 }
 
