@@ -60,6 +60,8 @@ BwdWorkspace bwd_workspace_layout(const Problem& p) {
   w.gate = off;    off = up(off + TH * 4);
   w.delta = off;   off = up(off + TH * 4);
   w.dsink_t = off; off = up(off + TH * 4);
+  w.sp = off;
+  off = up(off + static_cast<size_t>(p.T) * bwd_nbmax(p.W) * 64 * bwd_groups(p.H) * 128 * 2);
   w.total = off;
   return w;
 }
@@ -144,28 +146,31 @@ k_bwd_pre(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict
   }
 }
 
-// ------------------------------------------------------------------ b2-b6
+// ------------------------------------------------------------------ b2-b4: dq, dS', P
 
 constexpr int kHG = 32;                  // heads per CTA (UMMA N of S, dP, dQ)
 constexpr int kThreads = 256;
 constexpr int kProducers = 96;           // warps 5-7
 constexpr int kKVChunk = kBlk * 128;     // 16 KB
 constexpr int kHChunk = kHG * 128;       // 4 KB: 64 columns of 32 head rows
-// smem position p of the gathered block holds d-chunk x(p): p=0 rope, p=1..8 V chunks 0..7
+// smem position p of the gathered block holds d-chunk x(p): p = 0 the rope
+// columns 512..575 (reused for the P tile once the rope part of dQ is done),
+// p = 1..8 the V chunks 0..7.  Blocks are gathered and consumed in the order
+// p = 1..8, 0 because position 0 is released last.
 constexpr int kOffKV = 0;
 constexpr int kOffQ = kOffKV + kChunks * kKVChunk;  // 9 chunks, chunk x = d-chunk x
 constexpr int kOffdO = kOffQ + kChunks * kHChunk;   // 8 chunks
 constexpr int kOffdS = kOffdO + 8 * kHChunk;        // 2 sub-tiles of 64 slots
 constexpr int kOffMisc = kOffdS + 2 * kHChunk;
+constexpr int kOffP = kOffKV;                       // P tile in position 0
 
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColdP = 32, kColP = 64, kColdQ = 96, kColdKV = 256;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColdP = 32, kColdQ = 64;
 
 struct Misc {
   uint64_t kv_full[kChunks];
   uint64_t kv_free[kChunks];
-  uint64_t qd_full, s_full, ds_full, dsp_free, dq_done, mma_done;
-  uint64_t dkv_full[2], dkv_empty[2];
+  uint64_t qd_full, s_full, ds_full, rope_done, dsp_free, dq_done, mma_done;
   float lse2[kHG], gate[kHG], delta[kHG];
   uint32_t tmem_base;
   int abort_flag;
@@ -175,25 +180,37 @@ constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffQ % 1024 == 0 && kOffdO % 1024 == 0 && kOffdS % 1024 == 0, "alignment");
 
+template <unsigned int* kErr>
 __device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicCAS(&g_err_bwd, 0u, 0x1FFu);
+      atomicCAS(kErr, 0u, 0x1FFu);
       return;
     }
   }
 }
 
 __device__ __forceinline__ int dchunk_of_pos(int pos) { return pos == 0 ? 8 : pos - 1; }
+// Gather / S-GEMM order of the shared positions: V chunks first, rope last.
+__device__ __forceinline__ int pos_of_step(int i) { return i == kChunks - 1 ? 0 : i + 1; }
+
+// Byte offset of element (head row h, slot) in a [32 rows x 128 slots] bf16
+// tile kept as two 128B-swizzled sub-tiles of 64 slots: the layout of dS' and
+// P (K-major B for dQ^T; stored to the scratch by TMA, 32 rows x 64 slots
+// per box).
+__device__ __forceinline__ uint32_t hs_tile_off(uint32_t h, uint32_t slot) {
+  const uint32_t col = slot & 63u;
+  return (slot >> 6) * kHChunk + h * 128u + ((((col >> 3) ^ (h & 7u)) << 4) | ((col & 7u) << 1));
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
-k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-           const __nv_bfloat16* __restrict__ kv, const int32_t* __restrict__ idxc,
-           const int32_t* __restrict__ count, const float* __restrict__ lse2_g,
-           const float* __restrict__ gate_g, const float* __restrict__ delta_g,
-           float* __restrict__ dkv_acc, __nv_bfloat16* __restrict__ dq, int T, int H, int W,
-           float scale, int G, int box_heads) {
+k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+         const __grid_constant__ CUtensorMap tm_sp, const __nv_bfloat16* __restrict__ kv,
+         const int32_t* __restrict__ idxc, const int32_t* __restrict__ count,
+         const float* __restrict__ lse2_g, const float* __restrict__ gate_g,
+         const float* __restrict__ delta_g, __nv_bfloat16* __restrict__ dq, int T, int H, int W,
+         float scale, int G, int box_heads, int nbmax) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
@@ -208,7 +225,7 @@ k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   const FailState fs{&g_err_bwd, &m.abort_flag};
   const int Kt = count[t];
 
-  if (Kt == 0) {  // empty row: dq = 0, no dkv contribution
+  if (Kt == 0) {  // empty row: dq = 0, nothing for dkv
     for (int v = tid; v < nh * (kDqk / 8); v += kThreads) {
       const int h = v / (kDqk / 8), c = v - h * (kDqk / 8);
       *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kDqk + c * 8) =
@@ -227,13 +244,10 @@ k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     mbar_init(smem_u32(&m.qd_full), 1);
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.ds_full), 128);
+    mbar_init(smem_u32(&m.rope_done), 1);
     mbar_init(smem_u32(&m.dsp_free), 1);
     mbar_init(smem_u32(&m.dq_done), 1);
     mbar_init(smem_u32(&m.mma_done), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&m.dkv_full[i]), 1);
-      mbar_init(smem_u32(&m.dkv_empty[i]), 128);
-    }
     m.abort_flag = 0;
     mbar_init_fence();
   }
@@ -261,13 +275,13 @@ k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = m.tmem_base;
+  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
   if (warp >= 5) {
     // ------------------------------------------------------------ loads
-    // Q and dO tiles of the head group by TMA (K-major 64-column chunks of
-    // the head rows; heads past H inside the box are zero-filled), then the
-    // KV row gather with cp.async (one warp instruction = 4 whole 128 B row
-    // pieces) into the 128B-swizzled chunk tiles.
+    // Q and dO tiles of the head group by TMA, then the KV row gather with
+    // cp.async (one warp instruction = 4 whole 128 B row pieces) into the
+    // 128B-swizzled chunk tiles.
     const int pw = warp - 5;
     if (tid == 160) {
       mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kChunks + 8) * box_heads * 128);
@@ -277,7 +291,8 @@ k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         tma_load_3d(sbase + kOffdO + c * kHChunk, &tm_do, c * 64, h0, t, smem_u32(&m.qd_full));
     }
     for (int b = 0; b < nblk; ++b) {
-      for (int pos = 0; pos < kChunks; ++pos) {
+      for (int i = 0; i < kChunks; ++i) {
+        const int pos = pos_of_step(i);
         if (b > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (b - 1) & 1, fs, 1);
         const int x = dchunk_of_pos(pos);
         for (int g = pw; g < kBlk / 4; g += 3) {
@@ -297,12 +312,10 @@ k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     if (lane == 0) {
       const uint32_t idS = idesc_bf16(128, kHG, false, false);     // S^T, dP^T
       const uint32_t idQ = idesc_bf16(128, kHG, true, false);      // dQ^T: A MN-major, B K-major
-      const uint32_t idKV = idesc_bf16(128, 128, true, true);      // dS'^T . Q (V columns)
-      const uint32_t idKVr = idesc_bf16(128, 64, true, true);      // dS'^T . Q (rope columns)
-      const uint32_t idPT = idesc_bf16(128, 128, false, true);     // P^T (TMEM) . dO
       mbar_wait(smem_u32(&m.qd_full), 0, fs, 2);
       for (int b = 0; b < nblk; ++b) {
-        for (int pos = 0; pos < kChunks; ++pos) {
+        for (int i = 0; i < kChunks; ++i) {
+          const int pos = pos_of_step(i);
           mbar_wait(smem_u32(&m.kv_full[pos]), b & 1, fs, 3);
           fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
           tc_fence_after();
@@ -311,10 +324,10 @@ k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           for (int k = 0; k < 4; ++k) {
             const uint64_t a = sdesc_sw128(sbase + kOffKV + pos * kKVChunk + k * 32, 16, 1024);
             const uint64_t bq = sdesc_sw128(sbase + kOffQ + x * kHChunk + k * 32, 16, 1024);
-            umma_ss(tmem + kColS, a, bq, idS, (pos | k) != 0);
+            umma_ss(tmem + kColS, a, bq, idS, (i | k) != 0);
             if (x < 8) {
               const uint64_t bd = sdesc_sw128(sbase + kOffdO + x * kHChunk + k * 32, 16, 1024);
-              umma_ss(tmem + kColdP, a, bd, idS, (x | k) != 0);
+              umma_ss(tmem + kColdP, a, bd, idS, (i | k) != 0);
             }
           }
         }
@@ -335,126 +348,77 @@ k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             umma_ss(tmem + kColdQ + j * kHG, a, bs, idQ, (b | kk) != 0);
           }
           if (j == 4) {
-            umma_commit(smem_u32(&m.kv_free[0]));
+            umma_commit(smem_u32(&m.rope_done));
           } else {
             umma_commit(smem_u32(&m.kv_free[pos0]));
             umma_commit(smem_u32(&m.kv_free[pos0 + 1]));
           }
         }
-        // dKV tile for this block's 128 gathered rows, 5 column chunks.
-        for (int n = 0; n < 5; ++n) {
-          const int gidx = b * 5 + n, buf = gidx & 1, use = gidx >> 1;
-          if (use > 0) mbar_wait(smem_u32(&m.dkv_empty[buf]), (use - 1) & 1, fs, 5);
-          tc_fence_after();
-          const uint32_t d_t = tmem + kColdKV + buf * 128;
-          if (n < 4) {
-#pragma unroll
-            for (int kk = 0; kk < kHG / 16; ++kk) {
-              const uint64_t a = sdesc_sw128(sbase + kOffdS + kk * 2048, kHChunk, 1024);
-              const uint64_t bq =
-                  sdesc_sw128(sbase + kOffQ + (2 * n) * kHChunk + kk * 2048, kHChunk, 1024);
-              umma_ss(d_t, a, bq, idKV, kk != 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < kHG / 16; ++kk) {
-              const uint64_t bd =
-                  sdesc_sw128(sbase + kOffdO + (2 * n) * kHChunk + kk * 2048, kHChunk, 1024);
-              umma_ts(d_t, tmem + kColP + kk * 8, bd, idPT, 1);
-            }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < kHG / 16; ++kk) {
-              const uint64_t a = sdesc_sw128(sbase + kOffdS + kk * 2048, kHChunk, 1024);
-              const uint64_t bq = sdesc_sw128(sbase + kOffQ + 8 * kHChunk + kk * 2048, kHChunk, 1024);
-              umma_ss(d_t, a, bq, idKVr, kk != 0);
-            }
-          }
-          umma_commit(smem_u32(&m.dkv_full[buf]));
-        }
         umma_commit(smem_u32(&m.dsp_free));
       }
       umma_commit(smem_u32(&m.dq_done));
       umma_commit(smem_u32(&m.mma_done));
-      mbar_wait_final(smem_u32(&m.mma_done), 0);
+      mbar_wait_final<&g_err_bwd>(smem_u32(&m.mma_done), 0);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ dS / dKV drain / dQ store
+    // ------------------------------------------------------------ P, dS', dq
     const float sl2 = scale * kLog2e;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const size_t spr = static_cast<size_t>(64) * G;  // scratch rows per (token, block)
     for (int b = 0; b < nblk; ++b) {
-      mbar_wait(smem_u32(&m.s_full), b & 1, fs, 6);
+      mbar_wait(smem_u32(&m.s_full), b & 1, fs, 7);
       tc_fence_after();
       uint32_t rs[32], rd[32];
       tmem_ld32x2_sync(tmem + lane_base + kColS, rs, tmem + lane_base + kColdP, rd);
-      const int slot = b * kBlk + tid;
-      const bool valid = slot < Kt;
-      uint32_t pk[16];
-      float dsv[kHG];
+      const bool valid = b * kBlk + tid < Kt;
+      float pv[kHG], dsv[kHG];
 #pragma unroll
-      for (int i = 0; i < kHG / 2; ++i) {
-        float pv[2];
+      for (int h = 0; h < kHG; ++h) {
+        // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
+        const float p = valid ? exp2f(fmaf(__uint_as_float(rs[h]), sl2, -m.lse2[h])) * m.gate[h]
+                              : 0.f;
+        pv[h] = p;
+        dsv[h] = valid ? p * (__uint_as_float(rd[h]) - m.delta[h]) * scale : 0.f;
+      }
+      if (b > 0) mbar_wait(smem_u32(&m.dsp_free), (b - 1) & 1, fs, 8);
+      // thread 0 finished reading the previous block's tiles out (bulk wait below)
+      named_bar_sync(1, 128);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int h = 2 * i + e;
-          // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
-          const float p = valid ? exp2f(fmaf(__uint_as_float(rs[h]), sl2, -m.lse2[h])) * m.gate[h]
-                                : 0.f;
-          pv[e] = p;
-          dsv[h] = p * (__uint_as_float(rd[h]) - m.delta[h]) * scale;
-        }
-        pk[i] = pack_bf16x2(pv[0], pv[1]);
+      for (int h = 0; h < kHG; ++h) {
+        const __nv_bfloat16 v = __float2bfloat16_rn(dsv[h]);
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(sbase + kOffdS + hs_tile_off(h, tid)),
+                     "h"(*reinterpret_cast<const unsigned short*>(&v))
+                     : "memory");
       }
-      if (b > 0) {
-        mbar_wait(smem_u32(&m.dsp_free), (b - 1) & 1, fs, 7);
-        tc_fence_after();
-      }
-      tmem_st16(tmem + lane_base + kColP, pk);
-      {
-        // dS'^T tile: element (head h, slot) of a 32-row, 128-byte-swizzled tile per 64 slots.
-        const uint32_t sub = sbase + kOffdS + (tid >> 6) * kHChunk;
-        const uint32_t col = tid & 63;
-#pragma unroll
-        for (int h = 0; h < kHG; ++h) {
-          const uint32_t addr = sub + h * 128 + ((((col >> 3) ^ (h & 7)) << 4) | ((col & 7) << 1));
-          const __nv_bfloat16 v = __float2bfloat16_rn(dsv[h]);
-          asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
-                       "h"(*reinterpret_cast<const unsigned short*>(&v))
-                       : "memory");
-        }
-      }
-      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&m.ds_full));
-
-      // Scatter-add this block's dKV rows.
-      const int r = valid ? rows[slot] : -1;
-      float* dst_row = dkv_acc + static_cast<size_t>(r < 0 ? 0 : r) * kDqk;
-      for (int n = 0; n < 5; ++n) {
-        const int gidx = b * 5 + n, buf = gidx & 1, use = gidx >> 1;
-        mbar_wait(smem_u32(&m.dkv_full[buf]), use & 1, fs, 8);
-        tc_fence_after();
-        const int npieces = (n < 4) ? 4 : 2;
-        for (int pc = 0; pc < npieces; ++pc) {
-          uint32_t v[32];
-          tmem_ld32_sync(tmem + lane_base + kColdKV + buf * 128 + pc * 32, v);
-          if (r >= 0) {
-            float4* d4 = reinterpret_cast<float4*>(dst_row + n * 128 + pc * 32);
+      // P goes into position 0 once the rope part of dQ has read the rope rows.
+      mbar_wait(smem_u32(&m.rope_done), b & 1, fs, 9);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              atomicAdd(d4 + i, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                            __uint_as_float(v[4 * i + 2]),
-                                            __uint_as_float(v[4 * i + 3])));
-          }
+      for (int h = 0; h < kHG; ++h) {
+        const __nv_bfloat16 v = __float2bfloat16_rn(pv[h]);
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(sbase + kOffP + hs_tile_off(h, tid)),
+                     "h"(*reinterpret_cast<const unsigned short*>(&v))
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (tid == 0) {
+        // dS' and P rows of this head group -> the (token, block) scratch tile
+        const int row0 = static_cast<int>((static_cast<size_t>(t) * nbmax + b) * spr) + h0;
+        for (int half = 0; half < 2; ++half) {
+          tma_store_2d(&tm_sp, half * 64, row0, sbase + kOffdS + half * kHChunk);
+          tma_store_2d(&tm_sp, half * 64, row0 + 32 * G, sbase + kOffP + half * kHChunk);
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&m.dkv_empty[buf]));
+        bulk_commit();
+        bulk_wait_read();
+        mbar_arrive(smem_u32(&m.kv_free[0]));  // position 0 may take the next rope rows
       }
     }
 
-    // dQ^T -> dq (bf16), staged through shared memory for coalesced stores.
-    mbar_wait(smem_u32(&m.dq_done), 0, fs, 9);
+    // dQ^T -> dq (bf16), staged through shared memory for one bulk store.
+    mbar_wait(smem_u32(&m.dq_done), 0, fs, 10);
     tc_fence_after();
     __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV);  // [32][576]
     for (int j = 0; j < 5; ++j) {
@@ -479,6 +443,201 @@ k_bwd_main(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   if (warp == 4) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ b5-b6: dKV
+
+// One CTA per token, every head at once:
+//   dKV^T[d, slot] = sum_h Q[h, d] dS'[h, slot] + sum_h dO[h, d] P[h, slot]
+// M = 128 d rows per chunk (4 V chunks + the rope chunk), N = 128 slots of a
+// block, K = 32G heads of dS' plus 32G heads of P.  A = [Q^T | dO^T] chunk
+// (MN-major, from q/dout by 3-D TMA), B = the (token, block) scratch tile
+// written by k_bwd_dq (MN-major).  With d on the TMEM lanes, each warp-level
+// atomic adds 128 contiguous bytes of one KV row, and there is one partial per
+// valid slot, however many head groups there are.
+namespace dkv {
+constexpr int kDrainWarps = 16;             // 4 per sub-partition, 32 slots each
+constexpr int kThreads = (kDrainWarps + 2) * 32;
+constexpr int kTmaWarp = kDrainWarps, kMmaWarp = kDrainWarps + 1;
+constexpr int kBTile = 64 * 4 * 128 * 2;    // up to 256 rows x 128 slots bf16 = 64 KB
+constexpr int kAStage = 4 * 128 * 128;      // Q and dO, 2 boxes each of up to 128 heads x 64 d
+constexpr int kOffB = 0;
+constexpr int kOffA = kOffB + kBTile;       // 2 stages
+constexpr int kOffIdx = kOffA + 2 * kAStage;
+constexpr int kOffMisc = kOffIdx + kDrainWarps * 32 * 4;
+constexpr uint32_t kTmemCols = 256;         // 2 accumulators of 128 columns
+
+struct Misc {
+  uint64_t b_full, b_empty, a_full[2], a_empty[2], d_full[2], d_empty[2], mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffA % 1024 == 0, "alignment");
+}  // namespace dkv
+
+__global__ void __launch_bounds__(dkv::kThreads, 1)
+k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUtensorMap tm_doa,
+          const __grid_constant__ CUtensorMap tm_spb, const int32_t* __restrict__ idxc,
+          const int32_t* __restrict__ count, float* __restrict__ dkv_acc, int T, int H, int W,
+          int G, int box_heads, int nbmax) {
+  using dkv::kDrainWarps;
+  using dkv::kTmaWarp;
+  using dkv::kMmaWarp;
+  using dkv::kOffB;
+  using dkv::kOffA;
+  using dkv::kAStage;
+  using dkv::kOffIdx;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = blockIdx.x;
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {
+    if (tid == 0) atomicCAS(&g_err_bwd, 0u, 0x3FFu);
+    return;
+  }
+  const int Kt = count[t];
+  if (Kt == 0) return;
+  const int nblk = (Kt + kBlk - 1) / kBlk;
+  dkv::Misc& m = *reinterpret_cast<dkv::Misc*>(smem + dkv::kOffMisc);
+  const FailState fs{&g_err_bwd, &m.abort_flag};
+  const int HP = 32 * G;                          // padded head rows per half
+  const uint32_t a_half = static_cast<uint32_t>(HP) * 128;  // one 64-d box of HP rows
+  const uint32_t b_half = static_cast<uint32_t>(2 * HP) * 128;  // one 64-slot box
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&m.b_full), 1);
+    mbar_init(smem_u32(&m.b_empty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&m.a_full[i]), 1);
+      mbar_init(smem_u32(&m.a_empty[i]), 1);
+      mbar_init(smem_u32(&m.d_full[i]), 1);
+      mbar_init(smem_u32(&m.d_empty[i]), kDrainWarps * 32);
+    }
+    mbar_init(smem_u32(&m.mma_done), 1);
+    m.abort_flag = 0;
+    mbar_init_fence();
+  }
+  // A rows past H inside the padded head range stay zero (the TMA box covers
+  // only H rows): the matching scratch rows are zero, and 0 * garbage could
+  // be NaN.
+  if (box_heads < HP) {
+    for (int i = tid; i < 2 * 4 * (HP - box_heads) * 8; i += dkv::kThreads) {
+      const int per = (HP - box_heads) * 8;
+      const int sb = i / per, rem = i - sb * per;  // sb: stage * 4 + box
+      const int row = box_heads + rem / 8, pc = rem & 7;
+      const uint32_t base = sbase + kOffA + (sb >> 2) * kAStage + (sb & 3) * a_half;
+      asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(base + sw128_off(row, pc)),
+                   "r"(0u)
+                   : "memory");
+    }
+  }
+  fence_proxy_async_smem();
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(&m.tmem_base), dkv::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+  const size_t spr = static_cast<size_t>(2 * HP);
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      for (int b = 0; b < nblk; ++b) {
+        if (b > 0) mbar_wait(smem_u32(&m.b_empty), (b - 1) & 1, fs, 20);
+        mbar_arrive_expect_tx(smem_u32(&m.b_full), 2 * b_half);
+        const int row0 = static_cast<int>((static_cast<size_t>(t) * nbmax + b) * spr);
+        tma_load_2d(sbase + kOffB, &tm_spb, 0, row0, smem_u32(&m.b_full));
+        tma_load_2d(sbase + kOffB + b_half, &tm_spb, 64, row0, smem_u32(&m.b_full));
+        for (int n = 0; n < 5; ++n) {
+          const int u = b * 5 + n, st = u & 1, use = u >> 1;
+          if (use > 0) mbar_wait(smem_u32(&m.a_empty[st]), (use - 1) & 1, fs, 21);
+          const uint32_t base = sbase + kOffA + st * kAStage;
+          const int nd = n < 4 ? 2 : 1;  // 64-d boxes in this chunk
+          const uint32_t bytes = (n < 4 ? 4u : 1u) * box_heads * 128u;
+          mbar_arrive_expect_tx(smem_u32(&m.a_full[st]), bytes);
+          for (int k = 0; k < nd; ++k)
+            tma_load_3d(base + k * a_half, &tm_qa, n * 128 + k * 64, 0, t, smem_u32(&m.a_full[st]));
+          if (n < 4)
+            for (int k = 0; k < 2; ++k)
+              tma_load_3d(base + (2 + k) * a_half, &tm_doa, n * 128 + k * 64, 0, t,
+                          smem_u32(&m.a_full[st]));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      const uint32_t id = idesc_bf16(128, kBlk, true, true);
+      for (int b = 0; b < nblk; ++b) {
+        mbar_wait(smem_u32(&m.b_full), b & 1, fs, 22);
+        for (int n = 0; n < 5; ++n) {
+          const int u = b * 5 + n, st = u & 1, use = u >> 1;
+          mbar_wait(smem_u32(&m.a_full[st]), use & 1, fs, 23);
+          if (use > 0) mbar_wait(smem_u32(&m.d_empty[st]), (use - 1) & 1, fs, 24);
+          tc_fence_after();
+          const uint32_t base = sbase + kOffA + st * kAStage;
+          const uint32_t d_t = tmem + st * kBlk;
+          // dS' . Q part: A = Q^T (M = d), B = scratch rows 0..HP-1
+          for (int kk = 0; kk < HP / 16; ++kk) {
+            const uint64_t a = sdesc_sw128(base + kk * 2048, a_half, 1024);
+            const uint64_t bb = sdesc_sw128(sbase + kOffB + kk * 2048, b_half, 1024);
+            umma_ss(d_t, a, bb, id, kk != 0);
+          }
+          if (n < 4) {  // P . dO part: A = dO^T, B = scratch rows HP..2HP-1
+            for (int kk = 0; kk < HP / 16; ++kk) {
+              const uint64_t a = sdesc_sw128(base + 2 * a_half + kk * 2048, a_half, 1024);
+              const uint64_t bb =
+                  sdesc_sw128(sbase + kOffB + HP * 128 + kk * 2048, b_half, 1024);
+              umma_ss(d_t, a, bb, id, 1);
+            }
+          }
+          umma_commit(smem_u32(&m.a_empty[st]));
+          umma_commit(smem_u32(&m.d_full[st]));
+        }
+        umma_commit(smem_u32(&m.b_empty));
+      }
+      umma_commit(smem_u32(&m.mma_done));
+      mbar_wait_final<&g_err_bwd>(smem_u32(&m.mma_done), 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ drain
+    // Warp w reads TMEM lanes 32 (w % 4) .. +31 (d rows of the chunk) and
+    // slot columns 32 (w / 4) .. +31.
+    const int sp = warp & 3, quarter = warp >> 2;
+    const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
+    int32_t* ridx = reinterpret_cast<int32_t*>(smem + kOffIdx) + warp * 32;
+    const int32_t* rows = idxc + static_cast<size_t>(t) * W;
+    for (int b = 0; b < nblk; ++b) {
+      const int s0 = b * kBlk + quarter * 32;
+      const int nvalid = max(0, min(32, Kt - s0));
+      ridx[lane] = lane < nvalid ? rows[s0 + lane] : 0;
+      __syncwarp();
+      for (int n = 0; n < 5; ++n) {
+        const int u = b * 5 + n, st = u & 1, use = u >> 1;
+        mbar_wait(smem_u32(&m.d_full[st]), use & 1, fs, 25);
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32_sync(tmem + lane_base + st * kBlk + quarter * 32, v);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&m.d_empty[st]));
+        const int d = n * 128 + sp * 32 + lane;
+        if (n < 4 || d < kDqk) {
+          float* dst = dkv_acc + d;
+#pragma unroll
+          for (int s = 0; s < 32; ++s)
+            if (s < nvalid) atomicAdd(dst + static_cast<size_t>(ridx[s]) * kDqk, __uint_as_float(v[s]));
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, dkv::kTmemCols);
 }
 
 // ------------------------------------------------------------------ casts and reductions
@@ -528,8 +687,11 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
                        cudaStream_t s, int stages) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_bwd_dkv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dkv::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -559,15 +721,29 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     }
   }
   if ((stages & kBwdMain) && p.T > 0) {
-    const int G = (p.H + kHG - 1) / kHG;
-    CUtensorMap tm_q, tm_do;
+    const int G = bwd_groups(p.H), nbmax = bwd_nbmax(p.W);
+    __nv_bfloat16* sp = reinterpret_cast<__nv_bfloat16*>(base + L.sp);
+    const long long sp_rows = static_cast<long long>(p.T) * nbmax * 64 * G;
+    CUtensorMap tm_q, tm_do, tm_sp_st;
     const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
     e = make_head_tile_map(&tm_q, q, p.T, p.H, kDqk, box_heads);
     if (e == cudaSuccess) e = make_head_tile_map(&tm_do, dout, p.T, p.H, kDv, box_heads);
+    if (e == cudaSuccess) e = make_matrix_map(&tm_sp_st, sp, sp_rows, kBlk, 32);
     if (e != cudaSuccess) return e;
-    k_bwd_main<<<static_cast<unsigned>(static_cast<long long>(p.T) * G), kThreads, kSmemBytes, s>>>(
-        tm_q, tm_do, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2, gate, delta, acc,
-        static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, box_heads);
+    k_bwd_dq<<<static_cast<unsigned>(static_cast<long long>(p.T) * G), kThreads, kSmemBytes, s>>>(
+        tm_q, tm_do, tm_sp_st, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2, gate,
+        delta, static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, box_heads, nbmax);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tm_qa, tm_doa, tm_sp_ld;
+    const int HP = 32 * G;
+    const int box_all = p.H < HP ? p.H : HP;
+    e = make_head_tile_map(&tm_qa, q, p.T, p.H, kDqk, box_all);
+    if (e == cudaSuccess) e = make_head_tile_map(&tm_doa, dout, p.T, p.H, kDv, box_all);
+    if (e == cudaSuccess) e = make_matrix_map(&tm_sp_ld, sp, sp_rows, kBlk, 2 * HP);
+    if (e != cudaSuccess) return e;
+    k_bwd_dkv<<<static_cast<unsigned>(p.T), dkv::kThreads, dkv::kSmemBytes, s>>>(
+        tm_qa, tm_doa, tm_sp_ld, idxc, count, acc, p.T, p.H, p.W, G, box_all, nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

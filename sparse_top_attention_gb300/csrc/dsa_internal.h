@@ -23,8 +23,13 @@ struct BwdWorkspace {
   size_t gate;      // fp32 [T, H]    sigma(lse - sink), 0 for empty rows
   size_t delta;     // fp32 [T, H]    rowsum(dout * out)
   size_t dsink_t;   // fp32 [T, H]    -p_sink * delta
+  size_t sp;        // bf16 [T, nbmax, 64G, 128]: per (token, 128-slot block) the
+                    // dS' rows (32G heads) then the P rows (32G heads), slots
+                    // contiguous; G = ceil(H / 32), nbmax = ceil(W / 128)
   size_t total;
 };
+inline int bwd_groups(int H) { return (H + 31) / 32; }
+inline int bwd_nbmax(int W) { return (W + 127) / 128; }
 BwdWorkspace bwd_workspace_layout(const Problem& p);
 
 cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const int32_t* idx,

@@ -17,4 +17,9 @@ cudaError_t make_kv_gather_map(CUtensorMap* map, const void* kv, int rows);
 cudaError_t make_head_tile_map(CUtensorMap* map, const void* x, int T, int H, int width,
                                int box_heads);
 
+// 2-D map over a row-major bf16 matrix [rows, cols] with a 64-column x
+// `box_rows` box and 128-byte swizzle.
+cudaError_t make_matrix_map(CUtensorMap* map, const void* x, long long rows, int cols,
+                            int box_rows);
+
 }  // namespace dsa
