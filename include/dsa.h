@@ -161,6 +161,33 @@ dsa_status_t dsa_bwd_finalize(const dsa_problem_t* problem, const void* q, const
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * dsa_bwd without a workspace argument: the backward that allocates nothing.
+ * There is no counterpart on the pages; this is a convenience of this
+ * library.  It serves callers that cannot allocate device memory at call
+ * time:
+ *   - a plain C program that holds only its input and output buffers;
+ *   - a serving loop under a fixed memory budget, where a cudaMalloc would
+ *     synchronise the device.
+ * Arguments, outputs and errors are those of dsa_bwd.  The workspace comes
+ * from a fixed 64 MiB device array inside this library.  Every GPU that
+ * loads the library holds that array until the process exits.
+ *  - Size limit: if dsa_bwd_workspace_bytes(problem) exceeds 64 MiB, the
+ *    call returns DSA_ERR_WORKSPACE and launches nothing.  64 MiB covers,
+ *    for instance, T = 128 tokens at H = 128 with 640 slots per token.
+ *  - Set-up: the first call on a device looks up the array's device address
+ *    on the current device, once.  Make that first call before any stream
+ *    capture.
+ *  - Sharing: all calls share the one array, which keeps the last call's
+ *    contents (the call clears what must start at zero).  Calls that overlap
+ *    on the GPU, on different streams or from different threads, race on it.
+ *    Serialise them.
+ */
+dsa_status_t dsa_bwd_no_alloc(const dsa_problem_t* problem, const void* q, const void* kv,
+                              const int32_t* topk_idxs, const int32_t* topk_length,
+                              const float* sink, const void* out, const float* lse,
+                              const void* dout, void* dq, void* dkv, float* dsink, void* stream);
+
+/*
  * Slot decode and compaction: the first step of both passes, exposed so
  * that callers can check it bit-exactly.  For each token, the valid KV rows
  * are written to idx_out[t, 0:count) in slot order and the count to

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdsa.so")
-SOURCES = ["dsa_fwd.cu", "dsa_bwd.cu", "dsa_api.cu", "dsa_tmap.cu"]
+SOURCES = ["dsa_fwd.cu", "dsa_bwd.cu", "dsa_api.cu", "dsa_tmap.cu", "dsa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

@@ -28,8 +28,8 @@ STATUS = {
 
 # Every symbol that include/dsa.h declares.
 EXPORTS = ("dsa_fwd", "dsa_bwd_workspace_bytes", "dsa_bwd", "dsa_bwd_preprocess", "dsa_bwd_main",
-           "dsa_bwd_finalize", "dsa_topk_compact", "dsa_device_status", "dsa_status_string",
-           "dsa_version")
+           "dsa_bwd_finalize", "dsa_bwd_no_alloc", "dsa_topk_compact", "dsa_device_status",
+           "dsa_status_string", "dsa_version")
 BWD_STAGES = ("dsa_bwd_preprocess", "dsa_bwd_main", "dsa_bwd_finalize")
 FLAG_DELTA_RESIDUAL = 1
 
@@ -70,6 +70,9 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
         fn.argtypes = [prob, vp, vp, i32p, i32p, f32p, vp, f32p, vp, vp, vp, f32p, vp,
                        ctypes.c_size_t, vp]
         fn.restype = ctypes.c_int
+    lib.dsa_bwd_no_alloc.argtypes = [prob, vp, vp, i32p, i32p, f32p, vp, f32p, vp, vp, vp, f32p,
+                                     vp]
+    lib.dsa_bwd_no_alloc.restype = ctypes.c_int
     lib.dsa_topk_compact.argtypes = [prob, i32p, i32p, i32p, i32p, vp]
     lib.dsa_topk_compact.restype = ctypes.c_int
     lib.dsa_device_status.argtypes = [vp]
