@@ -13,8 +13,8 @@ Metrics:
   - value: fwd+bwd TFLOPS.  fwd FLOPs = 2*H*sum_t K_t*(576+512), with K_t the
     valid gathered slots; bwd = 2.5x fwd.
   - gathered-KV TB/s = sum_t K_t * 1152 B * 2 passes / step time.
-  - roofline: the dominant kernel (backward main) against the measured bf16
-    peak.
+  - roofline: the dominant kernel (k_bwd_dq, the dsa_bwd_main stage) against
+    the measured bf16 peak.
 
 `--impl reference` times the fp64 CPU oracle on the host cores.  Each step is
 a bounded sample of the same workload, scaled to the same unit.
@@ -40,7 +40,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 FWD_FLOPS_PER_SLOT_HEAD = 2 * (576 + 512)
-BWD_MAIN_FLOPS_PER_SLOT_HEAD = 2 * (576 + 512 + 576 + 576 + 512)  # S, dP, dQ, dK, dV
+BWD_DQ_FLOPS_PER_SLOT_HEAD = 2 * (576 + 512 + 576)   # k_bwd_dq: S, dP, dQ
+BWD_DKV_FLOPS_PER_SLOT_HEAD = 2 * (576 + 512)        # k_bwd_dkv: dK, dV
 ROW_BYTES = 576 * 2
 WORKLOAD = dict(name="flash_t8k", T=8192, H=128, topk=512, window=128, W=640, S_kv=8192 + 2048,
                 compact=False)
@@ -226,7 +227,8 @@ def run_ours(args, rank, world, local):
     T, H, S_kv, W = w.T, w.H, w.S_kv, w.W
     fwd_flops = FWD_FLOPS_PER_SLOT_HEAD * H * sum_k
     step_flops = 3.5 * fwd_flops
-    bwd_main_flops = BWD_MAIN_FLOPS_PER_SLOT_HEAD * H * sum_k
+    bwd_main_flops = BWD_DQ_FLOPS_PER_SLOT_HEAD * H * sum_k
+    bwd_dkv_flops = BWD_DKV_FLOPS_PER_SLOT_HEAD * H * sum_k
     gathered_bytes = 2 * ROW_BYTES * sum_k  # one gather list per token, fwd + bwd
 
     out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev)
@@ -295,7 +297,7 @@ def run_ours(args, rank, world, local):
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
-        traffic = json.load(open(tpath)).get("k_bwd_main")
+        traffic = json.load(open(tpath)).get("k_bwd_dq")
 
     # End to end through the public API: pinned host inputs -> device, fwd + bwd,
     # outputs -> pinned host, every step.
@@ -322,10 +324,11 @@ def run_ours(args, rank, world, local):
             "gathered_kv_tbps": world * gathered_bytes / (ms_step * 1e-3) / 1e12,
             "gathered_kv_frac_of_hbm": (gathered_bytes / (ms_step * 1e-3) / 1e9) / float(peaks["hbm_gbs"]),
             "frac_of_bf16_peak": value / world / peak,
-            "kernels_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms,
-                           "bwd_finalize": fin_ms},
+            "kernels_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main (k_bwd_dq)": main_ms,
+                           "bwd_finalize (k_bwd_dkv + cast + d_sink)": fin_ms},
             "fwd_tflops": fwd_tflops,
-            "roofline": {"kernel": "k_bwd_main", "bound": "tensor", "achieved": main_tflops,
+            "bwd_finalize_tflops": bwd_dkv_flops / (fin_ms * 1e-3) / 1e12,
+            "roofline": {"kernel": "k_bwd_dq", "bound": "tensor", "achieved": main_tflops,
                          "peak": peak, "unit": "TFLOP/s", "frac": main_tflops / peak,
                          "traffic": traffic, "peak_kind": f"bf16 sustained ({peak_kind})",
                          "flops_per_launch": bwd_main_flops},

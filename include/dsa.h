@@ -59,7 +59,7 @@ typedef enum {
 typedef struct {
   int32_t T;       /* query tokens, >= 0                                   */
   int32_t H;       /* query heads, 1..128                                  */
-  int32_t S_kv;    /* KV rows, >= 1                                        */
+  int32_t S_kv;    /* KV rows, 1..3728270 (576 * S_kv < 2^31)              */
   int32_t W;       /* index slots per token, >= 1                         */
   int32_t d_qk;    /* q/kv row width; must be 576                          */
   int32_t d_v;     /* V width (leading columns of kv); must be 512         */
@@ -126,7 +126,8 @@ size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem);
  * workspace: device memory of at least dsa_bwd_workspace_bytes(problem)
  * bytes, 256-byte aligned.  It is overwritten.
  * The call queues, in order: a memset, slot compaction, the delta
- * preprocess, the main kernel, the dkv cast, and the d_sink reduce.
+ * preprocess, the dq kernel, the dkv kernel, the dkv cast, and the d_sink
+ * reduce.
  */
 dsa_status_t dsa_bwd(const dsa_problem_t* problem, const void* q, const void* kv,
                      const int32_t* topk_idxs, const int32_t* topk_length, const float* sink,
@@ -140,9 +141,11 @@ dsa_status_t dsa_bwd(const dsa_problem_t* problem, const void* q, const void* kv
  * and with one workspace; together they equal one dsa_bwd call.
  *   dsa_bwd_preprocess  memset of the dkv accumulator, slot compaction and
  *                       the delta preprocess
- *   dsa_bwd_main        the main kernel: P recompute, dS, dq, dkv
- *                       scatter-add
- *   dsa_bwd_finalize    dkv fp32 -> bf16 cast and the d_sink reduce
+ *   dsa_bwd_main        P recompute, dS and dq for every 32-head group, which
+ *                       also stores the dS' and P tiles into the workspace
+ *   dsa_bwd_finalize    the dkv tile GEMM over all heads with its
+ *                       scatter-add, the dkv fp32 -> bf16 cast and the
+ *                       d_sink reduce
  */
 dsa_status_t dsa_bwd_preprocess(const dsa_problem_t* problem, const void* q, const void* kv,
                                 const int32_t* topk_idxs, const int32_t* topk_length,

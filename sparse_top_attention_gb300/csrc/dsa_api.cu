@@ -20,6 +20,8 @@ dsa_status_t check_problem(const dsa_problem_t* p) {
   if (!(p->scale == p->scale)) return DSA_ERR_INVALID_ARG;  // NaN scale
   if (p->d_qk != 576 || p->d_v != 512) return DSA_ERR_UNSUPPORTED;
   if (p->H > 128) return DSA_ERR_UNSUPPORTED;
+  // The backward addresses accumulator rows with 32-bit element offsets.
+  if (static_cast<int64_t>(p->S_kv) * 576 > INT32_MAX) return DSA_ERR_UNSUPPORTED;
   return DSA_OK;
 }
 

@@ -5,8 +5,11 @@
 //   k_compact   a1: valid KV rows of every token, in slot order, and counts
 //   k_bwd_pre   b1: delta = rowsum(dout * out), lse*log2(e), gate and the
 //               per-(t,h) d_sink terms (FlashAttention "dpsum" preprocess)
-//   k_bwd_main  b2-b6: per (token, 32-head group) recompute P, form dS,
-//               accumulate dQ in TMEM, scatter-add dKV rows with fp32 atomics
+//   k_bwd_dq    b2-b5: per (token, 32-head group) recompute P, form dS,
+//               accumulate dQ in TMEM and store dq; write the dS' and P
+//               tiles of every 128-slot block to a bf16 scratch
+//   k_bwd_dkv   b6: per token, dKV_blk^T = [Q^T | dO^T] [dS'; P] over all
+//               heads at once, scatter-added into the fp32 accumulator
 //   k_dkv_cast  fp32 accumulator -> bf16 dkv
 //   k_dsink     b7: d_sink[h] = sum_t (-p_sink * delta), fixed order
 //
@@ -30,16 +33,16 @@
 //     width > total_S_kv": a dkv contribution is judged by the index value
 //     and the top-k bound only.
 //
-// Main kernel tiles, transposed like the forward: gathered rows are UMMA M
+// k_bwd_dq tiles, transposed like the forward: gathered rows are UMMA M
 // (128) and the 32 heads of the group are N.
 //   S^T  = KV_blk . Q^T                  M=128 N=32  K=576   (smem x smem)
 //   dP^T = V_blk . dO^T                  M=128 N=32  K=512
 //   dQ^T += KV_blk^T . dS'^T             5 x (M=128 N=32 K=128)
-//   dKV_blk[:, 0:512]  = dS'^T Q + P^T dO   4 x (M=128 N=128 K=32+32)
-//   dKV_blk[:, 512:576] = dS'^T Q_rope      M=128 N=64 K=32
-// where dS' = scale * dS.  P^T is staged in TMEM as the A operand of its
-// GEMM.  dS'^T sits in one shared tile that serves as the K-major B of the
-// dQ GEMM and the MN-major A of the dKV GEMM.
+// where dS' = scale * dS.  dS'^T and P^T tiles are written to the scratch.
+// k_bwd_dkv tiles, per 128-slot block of one token, d rows on the M side:
+//   dKV_blk^T[d, slots] = [Q^T | dO^T][d, 2 x 32G] . [dS'; P][2 x 32G, slots]
+// (dO^T is zero for the 64 rope rows), so the dKV GEMM sees all heads at once
+// and each valid slot gets one partial per token.
 #include <cmath>
 
 #include "dsa_common.cuh"
@@ -284,25 +287,41 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     // 128B-swizzled chunk tiles.
     const int pw = warp - 5;
     if (tid == 160) {
+      const uint64_t pol = l2_evict_first();
       mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kChunks + 8) * box_heads * 128);
       for (int c = 0; c < kChunks; ++c)
-        tma_load_3d(sbase + kOffQ + c * kHChunk, &tm_q, c * 64, h0, t, smem_u32(&m.qd_full));
+        tma_load_3d_hint(sbase + kOffQ + c * kHChunk, &tm_q, c * 64, h0, t, smem_u32(&m.qd_full),
+                         pol);
       for (int c = 0; c < 8; ++c)
-        tma_load_3d(sbase + kOffdO + c * kHChunk, &tm_do, c * 64, h0, t, smem_u32(&m.qd_full));
+        tma_load_3d_hint(sbase + kOffdO + c * kHChunk, &tm_do, c * 64, h0, t,
+                         smem_u32(&m.qd_full), pol);
     }
+    const uint64_t keep = l2_evict_last();
     for (int b = 0; b < nblk; ++b) {
+      // This lane's rows of the block, read once (before the wait on the
+      // first chunk, so the reads overlap it) and reused by all 9 chunks.
+      const __nv_bfloat16* src[kRowGroups];
+      uint32_t dst[kRowGroups], nbytes[kRowGroups];
+#pragma unroll
+      for (int k = 0; k < kRowGroups; ++k) {
+        const int g = pw + 3 * k;
+        const int row = g * 4 + (lane >> 3), pc = lane & 7;
+        const int slot = b * kBlk + row;
+        const bool ok = g < kBlk / 4 && slot < Kt;
+        const int r = ok ? rows[slot] : 0;
+        src[k] = kv + static_cast<size_t>(r) * kDqk + pc * 8;
+        dst[k] = sw128_off(row & (kBlk - 1), pc);
+        nbytes[k] = ok ? 16u : 0u;
+      }
       for (int i = 0; i < kChunks; ++i) {
         const int pos = pos_of_step(i);
         if (b > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (b - 1) & 1, fs, 1);
         const int x = dchunk_of_pos(pos);
-        for (int g = pw; g < kBlk / 4; g += 3) {
-          const int row = g * 4 + (lane >> 3), pc = lane & 7;
-          const int slot = b * kBlk + row;
-          const bool ok = slot < Kt;
-          const int r = ok ? rows[slot] : 0;
-          cp_async_16(sbase + kOffKV + pos * kKVChunk + sw128_off(row, pc),
-                      kv + static_cast<size_t>(r) * kDqk + x * 64 + pc * 8, ok ? 16u : 0u);
-        }
+#pragma unroll
+        for (int k = 0; k < kRowGroups; ++k)
+          if (pw + 3 * k < kBlk / 4)
+            cp_async_16_hint(sbase + kOffKV + pos * kKVChunk + dst[k], src[k] + x * 64, nbytes[k],
+                             keep);
         cp_async_arrive(smem_u32(&m.kv_full[pos]));
       }
     }
@@ -407,9 +426,10 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       if (tid == 0) {
         // dS' and P rows of this head group -> the (token, block) scratch tile
         const int row0 = static_cast<int>((static_cast<size_t>(t) * nbmax + b) * spr) + h0;
+        const uint64_t pol = l2_evict_first();
         for (int half = 0; half < 2; ++half) {
-          tma_store_2d(&tm_sp, half * 64, row0, sbase + kOffdS + half * kHChunk);
-          tma_store_2d(&tm_sp, half * 64, row0 + 32 * G, sbase + kOffP + half * kHChunk);
+          tma_store_2d_hint(&tm_sp, half * 64, row0, sbase + kOffdS + half * kHChunk, pol);
+          tma_store_2d_hint(&tm_sp, half * 64, row0 + 32 * G, sbase + kOffP + half * kHChunk, pol);
         }
         bulk_commit();
         bulk_wait_read();
@@ -433,7 +453,8 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     fence_proxy_async_smem();
     named_bar_sync(1, 128);
     if (tid == 0) {  // dq rows (t, h0..h0+nh) are contiguous
-      bulk_store(dq + (static_cast<size_t>(t) * H + h0) * kDqk, smem_u32(stage), nh * kDqk * 2);
+      bulk_store_hint(dq + (static_cast<size_t>(t) * H + h0) * kDqk, smem_u32(stage),
+                      nh * kDqk * 2, l2_evict_first());
       bulk_commit();
       bulk_wait_read();
     }
@@ -547,8 +568,9 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         if (b > 0) mbar_wait(smem_u32(&m.b_empty), (b - 1) & 1, fs, 20);
         mbar_arrive_expect_tx(smem_u32(&m.b_full), 2 * b_half);
         const int row0 = static_cast<int>((static_cast<size_t>(t) * nbmax + b) * spr);
-        tma_load_2d(sbase + kOffB, &tm_spb, 0, row0, smem_u32(&m.b_full));
-        tma_load_2d(sbase + kOffB + b_half, &tm_spb, 64, row0, smem_u32(&m.b_full));
+        const uint64_t pol = l2_evict_first();
+        tma_load_2d_hint(sbase + kOffB, &tm_spb, 0, row0, smem_u32(&m.b_full), pol);
+        tma_load_2d_hint(sbase + kOffB + b_half, &tm_spb, 64, row0, smem_u32(&m.b_full), pol);
         for (int n = 0; n < 5; ++n) {
           const int u = b * 5 + n, st = u & 1, use = u >> 1;
           if (use > 0) mbar_wait(smem_u32(&m.a_empty[st]), (use - 1) & 1, fs, 21);
@@ -607,13 +629,14 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
     // slot columns 32 (w / 4) .. +31.
     const int sp = warp & 3, quarter = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
-    int32_t* ridx = reinterpret_cast<int32_t*>(smem + kOffIdx) + warp * 32;
     const int32_t* rows = idxc + static_cast<size_t>(t) * W;
+    const uint64_t keep = l2_evict_last();
     for (int b = 0; b < nblk; ++b) {
       const int s0 = b * kBlk + quarter * 32;
       const int nvalid = max(0, min(32, Kt - s0));
-      ridx[lane] = lane < nvalid ? rows[s0 + lane] : 0;
-      __syncwarp();
+      // Lane s holds the accumulator offset of slot s0 + s; shuffles hand it
+      // to the whole warp without a shared-memory round trip per add.
+      const uint32_t roff = lane < nvalid ? static_cast<uint32_t>(rows[s0 + lane]) * kDqk : 0u;
       for (int n = 0; n < 5; ++n) {
         const int u = b * 5 + n, st = u & 1, use = u >> 1;
         mbar_wait(smem_u32(&m.d_full[st]), use & 1, fs, 25);
@@ -626,8 +649,10 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         if (n < 4 || d < kDqk) {
           float* dst = dkv_acc + d;
 #pragma unroll
-          for (int s = 0; s < 32; ++s)
-            if (s < nvalid) atomicAdd(dst + static_cast<size_t>(ridx[s]) * kDqk, __uint_as_float(v[s]));
+          for (int s = 0; s < 32; ++s) {
+            const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
+            if (s < nvalid) red_add_f32_hint(dst + o, __uint_as_float(v[s]), keep);
+          }
         }
       }
       __syncwarp();
@@ -735,6 +760,11 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
         delta, static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, box_heads, nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+  }
+  if ((stages & kBwdFinal) && p.T > 0) {
+    const int G = bwd_groups(p.H), nbmax = bwd_nbmax(p.W);
+    __nv_bfloat16* sp = reinterpret_cast<__nv_bfloat16*>(base + L.sp);
+    const long long sp_rows = static_cast<long long>(p.T) * nbmax * 64 * G;
     CUtensorMap tm_qa, tm_doa, tm_sp_ld;
     const int HP = 32 * G;
     const int box_all = p.H < HP ? p.H : HP;

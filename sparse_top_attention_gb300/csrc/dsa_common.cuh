@@ -12,6 +12,8 @@ constexpr int kDv = 512;          // V = kv[:, :512]
 constexpr int kRowBytes = kDqk * 2;
 constexpr int kChunks = kDqk / 64;  // 64-column (128-byte) chunks of a row
 constexpr int kBlk = 128;         // gathered slots per block (UMMA M)
+// Rows of a block one gather warp issues: 3 warps share the 32 groups of 4 rows.
+constexpr int kRowGroups = (kBlk / 4 + 2) / 3;
 constexpr int kMaxW = 2048;       // index slots per token supported by the forward
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

@@ -139,8 +139,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
   // while the slots are decoded.
   if (tid == kQIssuer) {
     mbar_arrive_expect_tx(smem_u32(&m.q_full), kChunks * box_heads * 128);
+    const uint64_t pol = l2_evict_first();
     for (int c = 0; c < kChunks; ++c)
-      tma_load_3d(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t, smem_u32(&m.q_full));
+      tma_load_3d_hint(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t, smem_u32(&m.q_full),
+                       pol);
   }
 
   // a1: decode and compact the valid slots of token t (slot order).
@@ -175,17 +177,30 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
     // instruction moves 4 whole 128-byte row pieces.  Rows past the valid
     // count are zero-filled (their scores are masked).
     const int pw = warp - 5;
+    const uint64_t keep = l2_evict_last();
     for (int b = 0; b < nblk; ++b) {
+      // This lane's rows of the block, read once (before the wait on the
+      // first chunk, so the reads overlap it) and reused by all 9 chunks.
+      const __nv_bfloat16* src[kRowGroups];
+      uint32_t dst[kRowGroups], nbytes[kRowGroups];
+#pragma unroll
+      for (int k = 0; k < kRowGroups; ++k) {
+        const int g = pw + 3 * k;
+        const int row = g * 4 + (lane >> 3), pc = lane & 7;
+        const int slot = b * kBlk + row;
+        const bool ok = g < kBlk / 4 && slot < Kt;
+        const int r = ok ? list[slot] : 0;
+        src[k] = kv + static_cast<size_t>(r) * kDqk + pc * 8;
+        dst[k] = sw128_off(row & (kBlk - 1), pc);
+        nbytes[k] = ok ? 16u : 0u;
+      }
       for (int c = 0; c < kChunks; ++c) {
         if (b > 0) mbar_wait(smem_u32(&m.kv_free[c]), (b - 1) & 1, fs, 1);
-        for (int g = pw; g < kBlk / 4; g += 3) {
-          const int row = g * 4 + (lane >> 3), pc = lane & 7;
-          const int slot = b * kBlk + row;
-          const bool ok = slot < Kt;
-          const int r = ok ? list[slot] : 0;
-          cp_async_16(sbase + kOffKV + c * kKVChunk + sw128_off(row, pc),
-                      kv + static_cast<size_t>(r) * kDqk + c * 64 + pc * 8, ok ? 16u : 0u);
-        }
+#pragma unroll
+        for (int k = 0; k < kRowGroups; ++k)
+          if (pw + 3 * k < kBlk / 4)
+            cp_async_16_hint(sbase + kOffKV + c * kKVChunk + dst[k], src[k] + c * 64, nbytes[k],
+                             keep);
         cp_async_arrive(smem_u32(&m.kv_full[c]));
       }
     }
@@ -359,8 +374,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
     if (tid == 0) {
       // out rows (t, h0..h0+nh) are contiguous: one bulk store per half
       const size_t o = (static_cast<size_t>(t) * H + h0) * kDv;
-      bulk_store(out + o, smem_u32(stage), nh * kDv * 2);
-      if (residual) bulk_store(out + lo_off + o, smem_u32(stage_lo), nh * kDv * 2);
+      const uint64_t pol = l2_evict_first();
+      bulk_store_hint(out + o, smem_u32(stage), nh * kDv * 2, pol);
+      if (residual) bulk_store_hint(out + lo_off + o, smem_u32(stage_lo), nh * kDv * 2, pol);
       bulk_commit();
       bulk_wait_read();
     }
