@@ -394,7 +394,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 #pragma unroll
       for (int h = 0; h < kHG; ++h) {
         // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
-        const float p = valid ? exp2f(fmaf(__uint_as_float(rs[h]), sl2, -m.lse2[h])) * m.gate[h]
+        const float p = valid ? ex2_approx(fmaf(__uint_as_float(rs[h]), sl2, -m.lse2[h])) * m.gate[h]
                               : 0.f;
         pv[h] = p;
         dsv[h] = valid ? p * (__uint_as_float(rd[h]) - m.delta[h]) * scale : 0.f;

@@ -285,7 +285,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
         // Lazy rescale: keep the old shift unless the max grew by more than
         // 2^8; the final normalisation uses the same shift for O and l.
         resc = mn > mo + 8.f;
-        m.fac[tid] = resc ? exp2f(mo - mn) : 1.f;
+        m.fac[tid] = resc ? ex2_approx(mo - mn) : 1.f;
         if (resc) m.m_used[tid] = mn;
       }
       const bool any = named_bar_or(1, 128, resc);
@@ -297,8 +297,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = exp2f(s[2 * i] - m.m_used[2 * i]);
-        const float p1 = exp2f(s[2 * i + 1] - m.m_used[2 * i + 1]);
+        const float p0 = ex2_approx(s[2 * i] - m.m_used[2 * i]);
+        const float p1 = ex2_approx(s[2 * i + 1] - m.m_used[2 * i + 1]);
         lp[2 * i] += p0;
         lp[2 * i + 1] += p1;
         pk[i] = pack_bf16x2(p0, p1);

@@ -22,6 +22,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32): relative
+// error near 2^-22, results below 2^-126 flushed to +0, 2^-inf = +0.  The
+// softmax weights it feeds are rounded to bf16 or summed in fp32, far coarser
+// than that error.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
