@@ -23,19 +23,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-cudaError_t make_kv_gather_map(CUtensorMap* map, const void* kv, int rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return cudaErrorNotSupported;
-  cuuint64_t dims[2] = {576, static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {576 * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 cudaError_t make_head_tile_map(CUtensorMap* map, const void* x, int T, int H, int width,
                                int box_heads) {
   auto fn = encode_fn();

@@ -8,10 +8,6 @@
 
 namespace dsa {
 
-// 2-D map over kv [rows, 576] bf16 with a 64-column x 1-row box and 128-byte
-// swizzle: the map that tile::gather4 reads.
-cudaError_t make_kv_gather_map(CUtensorMap* map, const void* kv, int rows);
-
 // 3-D map over x [T, H, width] bf16 with a 64-column x `box_heads` x 1 box
 // and 128-byte swizzle: one K-major chunk of a head group per load.
 cudaError_t make_head_tile_map(CUtensorMap* map, const void* x, int T, int H, int width,
