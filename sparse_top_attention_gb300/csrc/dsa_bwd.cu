@@ -35,8 +35,7 @@
 //
 // k_bwd_dq tiles, transposed like the forward: gathered rows are UMMA M
 // (128) and the 32 heads of the group are N.
-//   S^T  = KV_blk . Q^T                  M=128 N=32  K=576   (smem x smem)
-//   dP^T = V_blk . dO^T                  M=128 N=32  K=512
+//   [S^T | dP^T] = KV_blk . [Q^T | dO^T]  M=128 N=64  K=512, then S^T += rope part (N=32, K=64)
 //   dQ^T += KV_blk^T . dS'^T             5 x (M=128 N=32 K=128)
 // where dS' = scale * dS.  dS'^T and P^T tiles are written to the scratch.
 // k_bwd_dkv tiles, per 128-slot block of one token, d rows on the M side:
@@ -161,9 +160,9 @@ constexpr int kHChunk = kHG * 128;       // 4 KB: 64 columns of 32 head rows
 // p = 1..8 the V chunks 0..7.  Blocks are gathered and consumed in the order
 // p = 1..8, 0 because position 0 is released last.
 constexpr int kOffKV = 0;
-constexpr int kOffQ = kOffKV + kChunks * kKVChunk;  // 9 chunks, chunk x = d-chunk x
-constexpr int kOffdO = kOffQ + kChunks * kHChunk;   // 8 chunks
-constexpr int kOffdS = kOffdO + 8 * kHChunk;        // 2 sub-tiles of 64 slots
+constexpr int kQdO = 2 * kHChunk;                   // Q chunk x, then dO chunk x
+constexpr int kOffQD = kOffKV + kChunks * kKVChunk;  // 8 (Q, dO) pairs, then the Q rope chunk
+constexpr int kOffdS = kOffQD + 8 * kQdO + kHChunk;  // 2 sub-tiles of 64 slots
 constexpr int kOffMisc = kOffdS + 2 * kHChunk;
 constexpr int kOffP = kOffKV;                       // P tile in position 0
 
@@ -181,7 +180,7 @@ struct Misc {
 
 constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffQ % 1024 == 0 && kOffdO % 1024 == 0 && kOffdS % 1024 == 0, "alignment");
+static_assert(kOffQD % 1024 == 0 && kOffdS % 1024 == 0, "alignment");
 
 template <unsigned int* kErr>
 __device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
@@ -267,8 +266,8 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     const int per = (kHG - box_heads) * 8;
     const int c = i / per, rem = i - c * per;
     const int row = box_heads + rem / 8, pc = rem & 7;
-    const uint32_t base = c < kChunks ? sbase + kOffQ + c * kHChunk
-                                      : sbase + kOffdO + (c - kChunks) * kHChunk;
+    const uint32_t base = c < kChunks ? sbase + kOffQD + c * kQdO
+                                      : sbase + kOffQD + (c - kChunks) * kQdO + kHChunk;
     asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(base + sw128_off(row, pc)), "r"(0u)
                  : "memory");
   }
@@ -290,10 +289,10 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       const uint64_t pol = l2_evict_first();
       mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kChunks + 8) * box_heads * 128);
       for (int c = 0; c < kChunks; ++c)
-        tma_load_3d_hint(sbase + kOffQ + c * kHChunk, &tm_q, c * 64, h0, t, smem_u32(&m.qd_full),
+        tma_load_3d_hint(sbase + kOffQD + c * kQdO, &tm_q, c * 64, h0, t, smem_u32(&m.qd_full),
                          pol);
       for (int c = 0; c < 8; ++c)
-        tma_load_3d_hint(sbase + kOffdO + c * kHChunk, &tm_do, c * 64, h0, t,
+        tma_load_3d_hint(sbase + kOffQD + c * kQdO + kHChunk, &tm_do, c * 64, h0, t,
                          smem_u32(&m.qd_full), pol);
     }
     const uint64_t keep = l2_evict_last();
@@ -329,7 +328,8 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   } else if (warp == 4) {
     // ------------------------------------------------------------ UMMA issue
     if (lane == 0) {
-      const uint32_t idS = idesc_bf16(128, kHG, false, false);     // S^T, dP^T
+      const uint32_t idSdP = idesc_bf16(128, 2 * kHG, false, false);  // [S^T | dP^T]
+      const uint32_t idS = idesc_bf16(128, kHG, false, false);         // S^T, rope part
       const uint32_t idQ = idesc_bf16(128, kHG, true, false);      // dQ^T: A MN-major, B K-major
       mbar_wait(smem_u32(&m.qd_full), 0, fs, 2);
       for (int b = 0; b < nblk; ++b) {
@@ -342,12 +342,10 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t a = sdesc_sw128(sbase + kOffKV + pos * kKVChunk + k * 32, 16, 1024);
-            const uint64_t bq = sdesc_sw128(sbase + kOffQ + x * kHChunk + k * 32, 16, 1024);
-            umma_ss(tmem + kColS, a, bq, idS, (i | k) != 0);
-            if (x < 8) {
-              const uint64_t bd = sdesc_sw128(sbase + kOffdO + x * kHChunk + k * 32, 16, 1024);
-              umma_ss(tmem + kColdP, a, bd, idS, (i | k) != 0);
-            }
+            // V chunks: S and dP in one N = 64 MMA (B rows: the Q heads, then the
+            // dO heads); the rope chunk adds to S only.
+            const uint64_t bqd = sdesc_sw128(sbase + kOffQD + x * kQdO + k * 32, 16, 1024);
+            umma_ss(tmem + kColS, a, bqd, x < 8 ? idSdP : idS, (i | k) != 0);
           }
         }
         umma_commit(smem_u32(&m.s_full));

@@ -288,6 +288,26 @@ __device__ __forceinline__ void tmem_ld32x2_sync(uint32_t ta, uint32_t (&r)[32],
       : "memory");
 }
 
+// Two 16-lane loads of an M = 64 accumulator (rows on lanes 0..15 of each
+// warp's quarter) and one wait.  Thread t < 16 gets lane t, columns
+// [c, c + 16); thread t >= 16 gets lane t - 16, columns [c + 16, c + 32).
+__device__ __forceinline__ void tmem_ld16x2_pair_sync(uint32_t ta, uint32_t (&r)[16], uint32_t tb,
+                                                      uint32_t (&q)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32], 16;\n\t"
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33], 16;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]),
+        "=r"(q[5]), "=r"(q[6]), "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]),
+        "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
