@@ -305,6 +305,28 @@ def run_ours(args, rank, world, local):
     if os.path.exists(tpath):
         traffic = json.load(open(tpath)).get("k_bwd_dq")
 
+    # The backward again with DSA_FLAG_DETERMINISTIC (bitwise reproducible
+    # dkv), all three stages, for the same steps.
+    ws_det = torch.empty(dsa.bwd_workspace_bytes(T, H, S_kv, W, deterministic=True),
+                         dtype=torch.uint8, device=dev)
+
+    def bwd_det():
+        dsa.bwd(w.q, w.kv, w.topk_idxs, None, w.sink, out, lse, w.dout, w.scale, dq=dq, dkv=dkv,
+                dsink=dsink, workspace=ws_det, deterministic=True)
+
+    for _ in range(args.warmup):
+        bwd_det()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    d0.record(stream)
+    for _ in range(args.steps):
+        bwd_det()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    assert dsa.device_status() == 0
+    bwd_det_ms = d0.elapsed_time(d1) / args.steps
+    del ws_det
+
     # End to end through the public API: pinned host inputs -> device, fwd + bwd,
     # outputs -> pinned host, every step.
     e2e = None
@@ -332,6 +354,8 @@ def run_ours(args, rank, world, local):
             "frac_of_bf16_peak": value / world / peak,
             "kernels_ms": {"fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main (k_bwd_dq)": main_ms,
                            "bwd_finalize (k_bwd_dkv + cast + d_sink)": fin_ms},
+            "bwd_ms": pre_ms + main_ms + fin_ms,
+            "bwd_deterministic_ms": bwd_det_ms,
             "fwd_tflops": fwd_tflops,
             "bwd_finalize_tflops": bwd_dkv_flops / (fin_ms * 1e-3) / 1e12,
             "roofline": {"kernel": "k_bwd_dq", "bound": "tensor", "achieved": main_tflops,

@@ -64,7 +64,7 @@ typedef struct {
   int32_t d_qk;    /* q/kv row width; must be 576                          */
   int32_t d_v;     /* V width (leading columns of kv); must be 512         */
   float scale;     /* softmax scale applied to q.kv (e.g. 1/sqrt(576))     */
-  uint32_t flags;  /* 0 or DSA_FLAG_DELTA_RESIDUAL                         */
+  uint32_t flags;  /* OR of DSA_FLAG_DELTA_RESIDUAL, DSA_FLAG_DETERMINISTIC  */
 } dsa_problem_t;
 
 /*
@@ -82,6 +82,22 @@ typedef struct {
  * The flag must be the same in the forward and the backward call.
  */
 #define DSA_FLAG_DELTA_RESIDUAL 1u
+
+/*
+ * DSA_FLAG_DETERMINISTIC: bitwise reproducible dkv (backward only).
+ * By default the backward scatter-adds each token's dkv rows with fp32
+ * atomics, so their order, and the last bits of dkv, change from run to
+ * run.  The pages name both designs (an atomic one on SM90 and a separate
+ * reduction on SM100).  With this flag the adds are 64-bit integer adds of
+ * round(v * 2^32).  Integer addition is order-independent, so dkv is the
+ * same bits every run; dq and d_sink are deterministic in both modes.
+ *   - Resolution 2^-32 (2.3e-10) per add; every dkv element must stay
+ *     below 2^31 in magnitude.
+ *   - The dkv accumulator in the workspace takes 8 bytes per element
+ *     instead of 4 (dsa_bwd_workspace_bytes accounts for it).
+ * Ignored by dsa_fwd.
+ */
+#define DSA_FLAG_DETERMINISTIC 2u
 
 /*
  * Forward.  Shapes and types (all device pointers):
@@ -103,10 +119,13 @@ dsa_status_t dsa_fwd(const dsa_problem_t* problem, const void* q, const void* kv
 /*
  * Bytes of device workspace that dsa_bwd needs for `problem`.  Returns 0 on
  * an invalid problem.  The workspace holds:
- *   - the fp32 dkv accumulator        [S_kv, 576];
+ *   - the dkv accumulator             [S_kv, 576], fp32 (int64 with
+ *                                     DSA_FLAG_DETERMINISTIC);
  *   - the compacted index lists       [T, W] and their counts [T];
  *   - per-(t,h) fp32 rows: lse*log2(e), sigma(lse - sink), delta and the
- *     d_sink terms.
+ *     d_sink terms;
+ *   - the dS'/P scratch that the main stage writes and the finalize stage
+ *     reads: bf16 [T, ceil(W / 128), 64 * ceil(H / 32), 128].
  */
 size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem);
 

@@ -16,7 +16,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 dsa_status_t check_problem(const dsa_problem_t* p) {
   if (p == nullptr) return DSA_ERR_INVALID_ARG;
   if (p->T < 0 || p->H < 1 || p->S_kv < 1 || p->W < 1) return DSA_ERR_INVALID_ARG;
-  if ((p->flags & ~DSA_FLAG_DELTA_RESIDUAL) != 0u) return DSA_ERR_INVALID_ARG;
+  if ((p->flags & ~(DSA_FLAG_DELTA_RESIDUAL | DSA_FLAG_DETERMINISTIC)) != 0u)
+    return DSA_ERR_INVALID_ARG;
   if (!(p->scale == p->scale)) return DSA_ERR_INVALID_ARG;  // NaN scale
   if (p->d_qk != 576 || p->d_v != 512) return DSA_ERR_UNSUPPORTED;
   if (p->H > 128) return DSA_ERR_UNSUPPORTED;
@@ -27,7 +28,8 @@ dsa_status_t check_problem(const dsa_problem_t* p) {
 
 dsa::Problem to_internal(const dsa_problem_t* p) {
   return dsa::Problem{p->T, p->H, p->S_kv, p->W, p->scale,
-                      (p->flags & DSA_FLAG_DELTA_RESIDUAL) != 0u};
+                      (p->flags & DSA_FLAG_DELTA_RESIDUAL) != 0u,
+                      (p->flags & DSA_FLAG_DETERMINISTIC) != 0u};
 }
 
 dsa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }

@@ -10,7 +10,8 @@
 //               tiles of every 128-slot block to a bf16 scratch
 //   k_bwd_dkv   b6: per token, dKV_blk^T = [Q^T | dO^T] [dS'; P] over all
 //               heads at once, scatter-added into the fp32 accumulator
-//   k_dkv_cast  fp32 accumulator -> bf16 dkv
+//   k_dkv_cast  fp32 accumulator -> bf16 dkv (k_dkv_cast_fixed for the int64
+//               fixed-point accumulator of DSA_FLAG_DETERMINISTIC)
 //   k_dsink     b7: d_sink[h] = sum_t (-p_sink * delta), fixed order
 //
 // Math per (t, h) and valid slot j.  The forward's lse excludes the sink;
@@ -55,7 +56,7 @@ BwdWorkspace bwd_workspace_layout(const Problem& p) {
   BwdWorkspace w{};
   size_t off = 0;
   const size_t TH = static_cast<size_t>(p.T) * p.H;
-  w.dkv_acc = off; off = up(off + static_cast<size_t>(p.S_kv) * kDqk * 4);
+  w.dkv_acc = off; off = up(off + static_cast<size_t>(p.S_kv) * kDqk * (p.deterministic ? 8 : 4));
   w.idxc = off;    off = up(off + static_cast<size_t>(p.T) * p.W * 4);
   w.count = off;   off = up(off + static_cast<size_t>(p.T) * 4);
   w.lse2 = off;    off = up(off + TH * 4);
@@ -482,8 +483,7 @@ constexpr int kBTile = 64 * 4 * 128 * 2;    // up to 256 rows x 128 slots bf16 =
 constexpr int kAStage = 4 * 128 * 128;      // Q and dO, 2 boxes each of up to 128 heads x 64 d
 constexpr int kOffB = 0;
 constexpr int kOffA = kOffB + kBTile;       // 2 stages
-constexpr int kOffIdx = kOffA + 2 * kAStage;
-constexpr int kOffMisc = kOffIdx + kDrainWarps * 32 * 4;
+constexpr int kOffMisc = kOffA + 2 * kAStage;
 constexpr uint32_t kTmemCols = 256;         // 2 accumulators of 128 columns
 
 struct Misc {
@@ -496,10 +496,13 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffA % 1024 == 0, "alignment");
 }  // namespace dkv
 
+// kDet: the accumulator is int64 in units of 2^-32 and the adds are integer
+// adds, so the sum does not depend on their order (bitwise reproducible).
+template <bool kDet>
 __global__ void __launch_bounds__(dkv::kThreads, 1)
 k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUtensorMap tm_doa,
           const __grid_constant__ CUtensorMap tm_spb, const int32_t* __restrict__ idxc,
-          const int32_t* __restrict__ count, float* __restrict__ dkv_acc, int T, int H, int W,
+          const int32_t* __restrict__ count, void* __restrict__ dkv_acc, int T, int H, int W,
           int G, int box_heads, int nbmax) {
   using dkv::kDrainWarps;
   using dkv::kTmaWarp;
@@ -507,7 +510,6 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
   using dkv::kOffB;
   using dkv::kOffA;
   using dkv::kAStage;
-  using dkv::kOffIdx;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x;
@@ -645,11 +647,20 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         mbar_arrive(smem_u32(&m.d_empty[st]));
         const int d = n * 128 + sp * 32 + lane;
         if (n < 4 || d < kDqk) {
-          float* dst = dkv_acc + d;
+          if constexpr (kDet) {
+            unsigned long long* dst = static_cast<unsigned long long*>(dkv_acc) + d;
 #pragma unroll
-          for (int s = 0; s < 32; ++s) {
-            const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
-            if (s < nvalid) red_add_f32_hint(dst + o, __uint_as_float(v[s]), keep);
+            for (int s = 0; s < 32; ++s) {
+              const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
+              if (s < nvalid) red_add_fixed32(dst + o, __uint_as_float(v[s]), keep);
+            }
+          } else {
+            float* dst = static_cast<float*>(dkv_acc) + d;
+#pragma unroll
+            for (int s = 0; s < 32; ++s) {
+              const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
+              if (s < nvalid) red_add_f32_hint(dst + o, __uint_as_float(v[s]), keep);
+            }
           }
         }
       }
@@ -676,6 +687,22 @@ k_dkv_cast(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dkv, long 
   o.y = pack_bf16x2(a.z, a.w);
   o.z = pack_bf16x2(b.x, b.y);
   o.w = pack_bf16x2(b.z, b.w);
+  reinterpret_cast<uint4*>(dkv)[i] = o;
+}
+
+// The fixed-point accumulator (int64, units of 2^-32) -> bf16 dkv.
+__global__ void __launch_bounds__(256)
+k_dkv_cast_fixed(const long long* __restrict__ acc, __nv_bfloat16* __restrict__ dkv, long long n8) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  float f[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) f[j] = fixed32_to_float(acc[8 * i + j]);
+  uint4 o;
+  o.x = pack_bf16x2(f[0], f[1]);
+  o.y = pack_bf16x2(f[2], f[3]);
+  o.z = pack_bf16x2(f[4], f[5]);
+  o.w = pack_bf16x2(f[6], f[7]);
   reinterpret_cast<uint4*>(dkv)[i] = o;
 }
 
@@ -713,21 +740,24 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     cudaError_t e = cudaFuncSetAttribute(k_bwd_dq, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_bwd_dkv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(k_bwd_dkv<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dkv::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_bwd_dkv<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                dkv::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const BwdWorkspace L = bwd_workspace_layout(p);
   uint8_t* base = static_cast<uint8_t*>(ws);
-  float* acc = reinterpret_cast<float*>(base + L.dkv_acc);
+  void* acc = base + L.dkv_acc;
   int32_t* idxc = reinterpret_cast<int32_t*>(base + L.idxc);
   int32_t* count = reinterpret_cast<int32_t*>(base + L.count);
   float* lse2 = reinterpret_cast<float*>(base + L.lse2);
   float* gate = reinterpret_cast<float*>(base + L.gate);
   float* delta = reinterpret_cast<float*>(base + L.delta);
   float* dsink_t = reinterpret_cast<float*>(base + L.dsink_t);
-  const size_t acc_bytes = static_cast<size_t>(p.S_kv) * kDqk * 4;
+  const size_t acc_bytes = static_cast<size_t>(p.S_kv) * kDqk * (p.deterministic ? 8 : 4);
   cudaError_t e = cudaSuccess;
   if (stages & kBwdPre) {
     e = cudaMemsetAsync(acc, 0, acc_bytes, s);
@@ -770,15 +800,20 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     if (e == cudaSuccess) e = make_head_tile_map(&tm_doa, dout, p.T, p.H, kDv, box_all);
     if (e == cudaSuccess) e = make_matrix_map(&tm_sp_ld, sp, sp_rows, kBlk, 2 * HP);
     if (e != cudaSuccess) return e;
-    k_bwd_dkv<<<static_cast<unsigned>(p.T), dkv::kThreads, dkv::kSmemBytes, s>>>(
+    auto kern = p.deterministic ? k_bwd_dkv<true> : k_bwd_dkv<false>;
+    kern<<<static_cast<unsigned>(p.T), dkv::kThreads, dkv::kSmemBytes, s>>>(
         tm_qa, tm_doa, tm_sp_ld, idxc, count, acc, p.T, p.H, p.W, G, box_all, nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdFinal) {
     const long long n8 = static_cast<long long>(p.S_kv) * kDqk / 8;
-    k_dkv_cast<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
-        acc, static_cast<__nv_bfloat16*>(dkv), n8);
+    if (p.deterministic)
+      k_dkv_cast_fixed<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
+          static_cast<const long long*>(acc), static_cast<__nv_bfloat16*>(dkv), n8);
+    else
+      k_dkv_cast<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
+          static_cast<const float*>(acc), static_cast<__nv_bfloat16*>(dkv), n8);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (dsink != nullptr) {

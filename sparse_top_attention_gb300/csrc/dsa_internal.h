@@ -12,11 +12,12 @@ struct Problem {
   int T, H, S_kv, W;
   float scale;
   bool delta_residual;  // out holds [2, T, H, 512]: rounded output, then its residual
+  bool deterministic;   // dkv summed as 64-bit fixed point (order-independent)
 };
 
 // Byte offsets inside the backward workspace (256-byte aligned pieces).
 struct BwdWorkspace {
-  size_t dkv_acc;   // fp32 [S_kv, 576]
+  size_t dkv_acc;   // fp32 [S_kv, 576], or int64 [S_kv, 576] in 2^-32 units when deterministic
   size_t idxc;      // int32 [T, W]   compacted rows
   size_t count;     // int32 [T]
   size_t lse2;      // fp32 [T, H]    lse * log2(e), 0 for empty rows

@@ -208,6 +208,19 @@ __device__ __forceinline__ void bulk_store_hint(void* gdst, uint32_t ssrc, uint3
                : "memory");
 }
 
+// Fixed-point accumulation in units of 2^-32 (two's complement in a u64):
+// v * 2^32 is exact in fp32 (a power-of-two scale), the conversion rounds to
+// the nearest integer (saturating beyond +-2^63), and integer adds commute,
+// so the final sum does not depend on the order of the adds.
+__device__ __forceinline__ void red_add_fixed32(unsigned long long* addr, float v, uint64_t pol) {
+  const long long q = __float2ll_rn(v * 4294967296.0f);
+  asm volatile("red.global.add.L2::cache_hint.u64 [%0], %1, %2;" ::"l"(addr), "l"(q), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ float fixed32_to_float(long long a) {
+  return __ll2float_rn(a) * 2.3283064365386963e-10f;  // 2^-32
+}
+
 // fp32 add into global memory without a return value, with an L2 policy.
 __device__ __forceinline__ void red_add_f32_hint(float* addr, float v, uint64_t pol) {
   asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(pol)

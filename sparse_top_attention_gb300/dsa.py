@@ -32,6 +32,7 @@ EXPORTS = ("dsa_fwd", "dsa_bwd_workspace_bytes", "dsa_bwd", "dsa_bwd_preprocess"
            "dsa_status_string", "dsa_version")
 BWD_STAGES = ("dsa_bwd_preprocess", "dsa_bwd_main", "dsa_bwd_finalize")
 FLAG_DELTA_RESIDUAL = 1
+FLAG_DETERMINISTIC = 2
 
 
 class Problem(ctypes.Structure):
@@ -177,19 +178,23 @@ def fwd(q, kv, topk_idxs, topk_length=None, sink=None, scale=None, out=None, lse
     return out, lse
 
 
-def bwd_workspace_bytes(T, H, S_kv, W, scale=1.0 / 24.0) -> int:
-    prob = make_problem(T, H, S_kv, W, scale)
+def bwd_workspace_bytes(T, H, S_kv, W, scale=1.0 / 24.0, deterministic=False) -> int:
+    prob = make_problem(T, H, S_kv, W, scale, FLAG_DETERMINISTIC if deterministic else 0)
     return int(library().dsa_bwd_workspace_bytes(ctypes.byref(prob)))
 
 
 def bwd(q, kv, topk_idxs, topk_length, sink, out, lse, dout, scale=None, dq=None, dkv=None,
-        dsink=None, workspace=None, stream=None, entry="dsa_bwd", delta_residual=False):
+        dsink=None, workspace=None, stream=None, entry="dsa_bwd", delta_residual=False,
+        deterministic=False):
     """Sparse MLA backward.  Returns (dq bf16, dkv bf16, dsink fp32 or None).
 
     ``entry`` selects ``dsa_bwd`` (all stages) or one of ``BWD_STAGES``.
-    ``delta_residual`` must match the forward call that produced ``out``."""
-    prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale,
-                                          FLAG_DELTA_RESIDUAL if delta_residual else 0)
+    ``delta_residual`` must match the forward call that produced ``out``.
+    ``deterministic`` (DSA_FLAG_DETERMINISTIC) makes dkv bitwise reproducible;
+    a caller-provided workspace must then be sized with the same flag."""
+    flags = (FLAG_DELTA_RESIDUAL if delta_residual else 0) | \
+        (FLAG_DETERMINISTIC if deterministic else 0)
+    prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale, flags)
     _need(q, "q", torch.bfloat16, (T, H, 576))
     _need(kv, "kv", torch.bfloat16, (S_kv, 576))
     _need(topk_idxs, "topk_idxs", torch.int32, (T, W))

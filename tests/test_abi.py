@@ -49,11 +49,14 @@ def test_workspace_size_is_pure_host(lib):
     assert n >= 5120 * 576 * 4 + 4096 * 640 * 4 + 4 * 4096 * 128 * 4
     assert n % 256 == 0
     assert lib.dsa_bwd_workspace_bytes(ctypes.byref(P(H=0))) == 0
+    # DSA_FLAG_DETERMINISTIC keeps dkv as int64: 4 more bytes per accumulator element
+    nd = lib.dsa_bwd_workspace_bytes(ctypes.byref(P(T=4096, H=128, S_kv=5120, W=640, flags=2)))
+    assert nd - n == 5120 * 576 * 4
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(H=0), 1), (dict(H=129), 2), (dict(T=-1), 1), (dict(W=0), 1), (dict(S_kv=0), 1),
-    (dict(d_qk=512), 2), (dict(d_v=576), 2), (dict(flags=2), 1), (dict(scale=float("nan")), 1),
+    (dict(d_qk=512), 2), (dict(d_v=576), 2), (dict(flags=4), 1), (dict(scale=float("nan")), 1),
     (dict(W=4096), 2), (dict(S_kv=3728271), 2),
 ])
 def test_forward_rejects_before_launch(lib, kw, code):
