@@ -210,6 +210,48 @@ dsa_status_t dsa_bwd_no_alloc(const dsa_problem_t* problem, const void* q, const
                               const void* dout, void* dq, void* dkv, float* dsink, void* stream);
 
 /*
+ * Varlen batches.  B sequences share the call: their tokens are packed
+ * along T and their KV rows along S_kv.
+ *   cu_seqlens_q   int32 [B + 1], device: sequence b holds tokens
+ *                  cu_seqlens_q[b] <= t < cu_seqlens_q[b + 1]
+ *                  (cu_seqlens_q[0] = 0, cu_seqlens_q[B] = T)
+ *   cu_seqlens_kv  int32 [B + 1], device: sequence b holds KV rows
+ *                  cu_seqlens_kv[b] <= r < cu_seqlens_kv[b + 1]
+ *                  (cu_seqlens_kv[0] = 0, cu_seqlens_kv[B] = S_kv)
+ * The cuDNN frontend's DSA kernel is batched: it reads topk_length per
+ * (batch, position) ("DSA backward SM90: fix three top-k and attention-sink
+ * boundary failures", Why 1); the other pages run B = 1.  A token's indices count from the first KV row of its own
+ * sequence: slot j is valid when 0 <= idx < (cu_seqlens_kv[b + 1] -
+ * cu_seqlens_kv[b]) and j < topk_length[t], and then names KV row
+ * cu_seqlens_kv[b] + idx.  The sink is per head, shared by all sequences;
+ * dkv covers all S_kv rows.  The offsets are read on the device only: they
+ * are expected to be non-decreasing; a token outside every sequence gets
+ * no valid slot, and ranges are clamped into [0, S_kv], so malformed offsets
+ * give wrong rows but never an access outside the tensors.
+ */
+typedef struct {
+  int32_t B;                     /* sequences, >= 1 */
+  const int32_t* cu_seqlens_q;   /* device, [B + 1], 4-byte aligned */
+  const int32_t* cu_seqlens_kv;  /* device, [B + 1], 4-byte aligned */
+} dsa_varlen_t;
+
+/*
+ * dsa_fwd and dsa_bwd for a varlen batch.  Arguments, layouts, outputs and
+ * errors are theirs, with T and S_kv the packed totals; `varlen` must not be
+ * NULL (DSA_ERR_INVALID_ARG).  The workspace of dsa_bwd_varlen is sized by
+ * dsa_bwd_workspace_bytes(problem) as for one sequence of the packed sizes.
+ */
+dsa_status_t dsa_fwd_varlen(const dsa_problem_t* problem, const dsa_varlen_t* varlen,
+                            const void* q, const void* kv, const int32_t* topk_idxs,
+                            const int32_t* topk_length, const float* sink, void* out, float* lse,
+                            void* stream);
+dsa_status_t dsa_bwd_varlen(const dsa_problem_t* problem, const dsa_varlen_t* varlen,
+                            const void* q, const void* kv, const int32_t* topk_idxs,
+                            const int32_t* topk_length, const float* sink, const void* out,
+                            const float* lse, const void* dout, void* dq, void* dkv, float* dsink,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Slot decode and compaction: the first step of both passes, exposed so
  * that callers can check it bit-exactly.  For each token, the valid KV rows
  * are written to idx_out[t, 0:count) in slot order and the count to

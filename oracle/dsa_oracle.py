@@ -38,6 +38,10 @@ Readings where the pages are silent (each also listed in the design notes):
   term and its own dkv contribution, which is what a gather computes.
 * The backward's delta uses the output the caller hands in when ``out`` is
   given.  Otherwise it uses the oracle's own fp64 O.
+* Varlen batches [P2 Why 1 reads topk_length per (batch, position)]: the
+  sequences are packed along T and along the KV rows; each sequence is the
+  single-sequence definition on its own slices, with its indices counted
+  from its own first KV row.  The sink is shared by all sequences.
 """
 from __future__ import annotations
 
@@ -212,6 +216,53 @@ def backward(q, kv, topk_idxs, topk_length, sink, scale, dout, d_v=512, out=None
             np.add.at(dkv, sel, contrib)
         dsink += dsink_t
     return {"dq": dq, "dkv": dkv, "dsink": dsink, "delta": delta_all}
+
+
+def _sequences(cu_seqlens_q, cu_seqlens_kv):
+    cq, ck = _np_int(cu_seqlens_q), _np_int(cu_seqlens_kv)
+    return [(int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])) for b in range(cq.size - 1)]
+
+
+def forward_varlen(q, kv, topk_idxs, topk_length, sink, scale, cu_seqlens_q, cu_seqlens_kv,
+                   d_v=512):
+    """A varlen batch: sequence b is tokens cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+    with KV rows cu_seqlens_kv[b] .. cu_seqlens_kv[b+1]-1, and its indices count
+    from its own first row.  Each sequence is ``forward`` on its slices."""
+    T, H, _ = q.shape
+    out = np.full((T, H, d_v), np.nan)
+    lse = np.full((T, H), np.nan)
+    count = np.full(T, -1, dtype=np.int64)
+    length = _np_int(topk_length)
+    for t0, t1, r0, r1 in _sequences(cu_seqlens_q, cu_seqlens_kv):
+        if t1 == t0:
+            continue
+        ref = forward(q[t0:t1], _np64(kv)[r0:r1], _np_int(topk_idxs)[t0:t1],
+                      None if length is None else length[t0:t1], sink, scale, d_v)
+        out[t0:t1], lse[t0:t1], count[t0:t1] = ref["out"], ref["lse"], ref["count"]
+    return {"out": out, "lse": lse, "count": count}
+
+
+def backward_varlen(q, kv, topk_idxs, topk_length, sink, scale, dout, cu_seqlens_q,
+                    cu_seqlens_kv, d_v=512, out=None):
+    """Gradients of a varlen batch: ``backward`` per sequence; dkv rows of a
+    sequence receive only its own tokens' contributions, and dsink sums over
+    all sequences."""
+    T, H, D = q.shape
+    kv64 = _np64(kv)
+    dq = np.full((T, H, D), np.nan)
+    dkv = np.zeros(kv64.shape)
+    dsink = np.zeros(H)
+    length = _np_int(topk_length)
+    for t0, t1, r0, r1 in _sequences(cu_seqlens_q, cu_seqlens_kv):
+        if t1 == t0:
+            continue
+        g = backward(q[t0:t1], kv64[r0:r1], _np_int(topk_idxs)[t0:t1],
+                     None if length is None else length[t0:t1], sink, scale, dout[t0:t1], d_v,
+                     out=None if out is None else out[t0:t1])
+        dq[t0:t1] = g["dq"]
+        dkv[r0:r1] += g["dkv"]
+        dsink += g["dsink"]
+    return {"dq": dq, "dkv": dkv, "dsink": dsink}
 
 
 def tokens_referencing(topk_idxs, topk_length, S_kv, rows):

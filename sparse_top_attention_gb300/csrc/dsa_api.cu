@@ -34,14 +34,33 @@ dsa::Problem to_internal(const dsa_problem_t* p) {
 
 dsa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
 
+// A varlen batch: B >= 1 sequences, both offset arrays given and 4-byte
+// aligned.  Their contents stay on the device; the kernels clamp them.
+dsa_status_t apply_varlen(const dsa_varlen_t* v, dsa::Problem* p) {
+  if (v == nullptr) return DSA_OK;
+  if (v->B < 1 || v->cu_seqlens_q == nullptr || v->cu_seqlens_kv == nullptr)
+    return DSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(v->cu_seqlens_q) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(v->cu_seqlens_kv) & 3u) != 0)
+    return DSA_ERR_ALIGNMENT;
+  p->cu_q = v->cu_seqlens_q;
+  p->cu_kv = v->cu_seqlens_kv;
+  p->B = v->B;
+  return DSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-dsa_status_t dsa_fwd(const dsa_problem_t* problem, const void* q, const void* kv,
-                     const int32_t* topk_idxs, const int32_t* topk_length, const float* sink,
-                     void* out, float* lse, void* stream) {
+static dsa_status_t fwd_impl(const dsa_problem_t* problem, const dsa_varlen_t* varlen,
+                             const void* q, const void* kv, const int32_t* topk_idxs,
+                             const int32_t* topk_length, const float* sink, void* out, float* lse,
+                             void* stream) {
   dsa_status_t st = check_problem(problem);
+  if (st != DSA_OK) return st;
+  dsa::Problem p = to_internal(problem);
+  st = apply_varlen(varlen, &p);
   if (st != DSA_OK) return st;
   if (problem->W > kMaxWForward) return DSA_ERR_UNSUPPORTED;
   if (problem->T == 0) return DSA_OK;
@@ -49,8 +68,22 @@ dsa_status_t dsa_fwd(const dsa_problem_t* problem, const void* q, const void* kv
   if (!aligned16(q) || !aligned16(kv) || !aligned16(topk_idxs) || !aligned16(out) ||
       !aligned16(lse) || (topk_length && !aligned16(topk_length)) || (sink && !aligned16(sink)))
     return DSA_ERR_ALIGNMENT;
-  return from_cuda(dsa::launch_fwd(to_internal(problem), q, kv, topk_idxs, topk_length, sink, out,
-                                   lse, static_cast<cudaStream_t>(stream)));
+  return from_cuda(dsa::launch_fwd(p, q, kv, topk_idxs, topk_length, sink, out, lse,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+dsa_status_t dsa_fwd(const dsa_problem_t* problem, const void* q, const void* kv,
+                     const int32_t* topk_idxs, const int32_t* topk_length, const float* sink,
+                     void* out, float* lse, void* stream) {
+  return fwd_impl(problem, nullptr, q, kv, topk_idxs, topk_length, sink, out, lse, stream);
+}
+
+dsa_status_t dsa_fwd_varlen(const dsa_problem_t* problem, const dsa_varlen_t* varlen,
+                            const void* q, const void* kv, const int32_t* topk_idxs,
+                            const int32_t* topk_length, const float* sink, void* out, float* lse,
+                            void* stream) {
+  if (varlen == nullptr) return DSA_ERR_INVALID_ARG;
+  return fwd_impl(problem, varlen, q, kv, topk_idxs, topk_length, sink, out, lse, stream);
 }
 
 size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem) {
@@ -62,14 +95,17 @@ static dsa_status_t bwd_stages(const dsa_problem_t* problem, const void* q, cons
                                const int32_t* topk_idxs, const int32_t* topk_length,
                                const float* sink, const void* out, const float* lse,
                                const void* dout, void* dq, void* dkv, float* dsink,
-                               void* workspace, size_t workspace_bytes, void* stream, int stages) {
+                               void* workspace, size_t workspace_bytes, void* stream, int stages,
+                               const dsa_varlen_t* varlen = nullptr) {
   dsa_status_t st = check_problem(problem);
+  if (st != DSA_OK) return st;
+  dsa::Problem p = to_internal(problem);
+  st = apply_varlen(varlen, &p);
   if (st != DSA_OK) return st;
   if (!kv || !dkv) return DSA_ERR_INVALID_ARG;
   if ((sink == nullptr) != (dsink == nullptr)) return DSA_ERR_INVALID_ARG;
   if (problem->T > 0 && (!q || !topk_idxs || !out || !lse || !dout || !dq))
     return DSA_ERR_INVALID_ARG;
-  const dsa::Problem p = to_internal(problem);
   const size_t need = dsa::bwd_workspace_layout(p).total;
   if (workspace == nullptr || workspace_bytes < need) return DSA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DSA_ERR_ALIGNMENT;
@@ -93,6 +129,15 @@ dsa_status_t dsa_bwd(DSA_BWD_ARGS_DECL) { return bwd_stages(DSA_BWD_ARGS, dsa::k
 dsa_status_t dsa_bwd_preprocess(DSA_BWD_ARGS_DECL) { return bwd_stages(DSA_BWD_ARGS, dsa::kBwdPre); }
 dsa_status_t dsa_bwd_main(DSA_BWD_ARGS_DECL) { return bwd_stages(DSA_BWD_ARGS, dsa::kBwdMain); }
 dsa_status_t dsa_bwd_finalize(DSA_BWD_ARGS_DECL) { return bwd_stages(DSA_BWD_ARGS, dsa::kBwdFinal); }
+
+dsa_status_t dsa_bwd_varlen(const dsa_problem_t* problem, const dsa_varlen_t* varlen,
+                            const void* q, const void* kv, const int32_t* topk_idxs,
+                            const int32_t* topk_length, const float* sink, const void* out,
+                            const float* lse, const void* dout, void* dq, void* dkv, float* dsink,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (varlen == nullptr) return DSA_ERR_INVALID_ARG;
+  return bwd_stages(DSA_BWD_ARGS, dsa::kBwdAll, varlen);
+}
 
 dsa_status_t dsa_topk_compact(const dsa_problem_t* problem, const int32_t* topk_idxs,
                               const int32_t* topk_length, int32_t* idx_out, int32_t* count_out,

@@ -79,11 +79,13 @@ constexpr int kCompactThreads = 256;
 
 __global__ void __launch_bounds__(kCompactThreads)
 k_compact(const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
-          int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out, int W, int S_kv) {
+          int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out, int W, int S_kv,
+          const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv, int B) {
   __shared__ int warp_counts[kCompactThreads / 32];
   const int t = blockIdx.x;
   const int len = slot_len(topk_length, t, W);
-  const int n = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, S_kv,
+  const KvRange kvr = kv_range(cu_q, cu_kv, B, t, S_kv);
+  const int n = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, kvr,
                               idx_out + static_cast<size_t>(t) * W, W, warp_counts, threadIdx.x,
                               kCompactThreads);
   if (threadIdx.x == 0) count_out[t] = n;
@@ -727,7 +729,8 @@ k_dsink(const float* __restrict__ dsink_t, float* __restrict__ dsink, int T, int
 cudaError_t launch_compact(const Problem& p, const int32_t* idx, const int32_t* len,
                            int32_t* idx_out, int32_t* count_out, cudaStream_t s) {
   if (p.T == 0) return cudaSuccess;
-  k_compact<<<p.T, kCompactThreads, 0, s>>>(idx, len, idx_out, count_out, p.W, p.S_kv);
+  k_compact<<<p.T, kCompactThreads, 0, s>>>(idx, len, idx_out, count_out, p.W, p.S_kv, p.cu_q,
+                                            p.cu_kv, p.B);
   return cudaGetLastError();
 }
 

@@ -36,12 +36,37 @@ __device__ __forceinline__ int slot_len(const int32_t* topk_length, int t, int W
   return n < 0 ? 0 : (n > W ? W : n);
 }
 
+// The KV rows a token may index: all S_kv rows, or in a varlen batch the rows
+// of the token's own sequence.  Sequence b holds tokens cu_q[b] <= t <
+// cu_q[b + 1] and KV rows cu_kv[b] <= r < cu_kv[b + 1]; its indices count
+// from cu_kv[b].  The range is clamped into [0, S_kv], and a token outside
+// every sequence gets an empty range, so malformed arrays cannot reach
+// outside kv.
+struct KvRange {
+  int lo, n;
+};
+__device__ __forceinline__ KvRange kv_range(const int32_t* cu_q, const int32_t* cu_kv, int B, int t,
+                                            int S_kv) {
+  if (cu_q == nullptr) return {0, S_kv};
+  int lo = 0, hi = B - 1;  // the last sequence whose first token is <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu_q[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  if (t < cu_q[lo] || t >= cu_q[lo + 1]) return {0, 0};
+  const int a = min(max(cu_kv[lo], 0), S_kv);
+  const int e = min(max(cu_kv[lo + 1], a), S_kv);
+  return {a, e - a};
+}
+
 // Block-wide compaction of one token's valid rows, in slot order.
 // All `nthreads` threads (a multiple of 32) must call it.  `warp_counts`
 // is shared scratch of nthreads/32 ints.  Writes up to `cap` entries to
-// `list` (shared or global) and returns the total valid count.
+// `list` (shared or global) and returns the total valid count.  Slot j is
+// valid when 0 <= idx < kv.n; its entry is the KV row kv.lo + idx.
 __device__ __forceinline__ int compact_token(const int32_t* __restrict__ idx_row, int W, int len,
-                                             int S_kv, int32_t* list, int cap, int* warp_counts,
+                                             KvRange kv, int32_t* list, int cap, int* warp_counts,
                                              int tid, int nthreads) {
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
@@ -52,7 +77,7 @@ __device__ __forceinline__ int compact_token(const int32_t* __restrict__ idx_row
     bool ok = false;
     if (j < W) {
       v = idx_row[j];
-      ok = slot_valid(v, j, len, S_kv);
+      ok = slot_valid(v, j, len, kv.n);
     }
     const unsigned bal = __ballot_sync(0xffffffffu, ok);
     if (lane == 0) warp_counts[warp] = __popc(bal);
@@ -64,7 +89,7 @@ __device__ __forceinline__ int compact_token(const int32_t* __restrict__ idx_row
       tot += c;
     }
     const int pos = off + __popc(bal & lt_mask);
-    if (ok && pos < cap) list[pos] = v;
+    if (ok && pos < cap) list[pos] = kv.lo + v;
     base += tot;
     __syncthreads();
   }

@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
            const float* __restrict__ sink, __nv_bfloat16* __restrict__ out,
            float* __restrict__ lse, const __nv_bfloat16* __restrict__ kv, int T, int H, int S_kv,
-           int W, float scale, int G, int residual, int box_heads) {
+           int W, float scale, int G, int residual, int box_heads,
+           const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv, int B) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
@@ -147,7 +148,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
 
   // a1: decode and compact the valid slots of token t (slot order).
   const int len = slot_len(topk_length, t, W);
-  const int Kt = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, S_kv, list, kMaxW,
+  const KvRange kvr = kv_range(cu_q, cu_kv, B, t, S_kv);
+  const int Kt = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, kvr, list, kMaxW,
                                m.warp_counts, tid, kThreads);
 
   const size_t lo_off = residual ? static_cast<size_t>(T) * H * kDv : 0;  // residual half
@@ -410,7 +412,7 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const in
   fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(
       tm_q, idx, len, sink, static_cast<__nv_bfloat16*>(out), lse,
       static_cast<const __nv_bfloat16*>(kv), p.T, p.H, p.S_kv, p.W, p.scale, G,
-      p.delta_residual ? 1 : 0, box_heads);
+      p.delta_residual ? 1 : 0, box_heads, p.cu_q, p.cu_kv, p.B);
   return cudaGetLastError();
 }
 

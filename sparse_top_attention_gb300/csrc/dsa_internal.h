@@ -13,6 +13,10 @@ struct Problem {
   float scale;
   bool delta_residual;  // out holds [2, T, H, 512]: rounded output, then its residual
   bool deterministic;   // dkv summed as 64-bit fixed point (order-independent)
+  // Varlen batch (device arrays of B + 1 offsets), or nullptr for one sequence.
+  const int32_t* cu_q = nullptr;
+  const int32_t* cu_kv = nullptr;
+  int B = 0;
 };
 
 // Byte offsets inside the backward workspace (256-byte aligned pieces).

@@ -28,11 +28,16 @@ STATUS = {
 
 # Every symbol that include/dsa.h declares.
 EXPORTS = ("dsa_fwd", "dsa_bwd_workspace_bytes", "dsa_bwd", "dsa_bwd_preprocess", "dsa_bwd_main",
-           "dsa_bwd_finalize", "dsa_bwd_no_alloc", "dsa_topk_compact", "dsa_device_status",
-           "dsa_status_string", "dsa_version")
+           "dsa_bwd_finalize", "dsa_bwd_no_alloc", "dsa_fwd_varlen", "dsa_bwd_varlen",
+           "dsa_topk_compact", "dsa_device_status", "dsa_status_string", "dsa_version")
 BWD_STAGES = ("dsa_bwd_preprocess", "dsa_bwd_main", "dsa_bwd_finalize")
 FLAG_DELTA_RESIDUAL = 1
 FLAG_DETERMINISTIC = 2
+
+
+class Varlen(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("cu_seqlens_q", ctypes.c_void_p),
+                ("cu_seqlens_kv", ctypes.c_void_p)]
 
 
 class Problem(ctypes.Structure):
@@ -74,6 +79,12 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.dsa_bwd_no_alloc.argtypes = [prob, vp, vp, i32p, i32p, f32p, vp, f32p, vp, vp, vp, f32p,
                                      vp]
     lib.dsa_bwd_no_alloc.restype = ctypes.c_int
+    vl = ctypes.POINTER(Varlen)
+    lib.dsa_fwd_varlen.argtypes = [prob, vl, vp, vp, i32p, i32p, f32p, vp, f32p, vp]
+    lib.dsa_fwd_varlen.restype = ctypes.c_int
+    lib.dsa_bwd_varlen.argtypes = [prob, vl, vp, vp, i32p, i32p, f32p, vp, f32p, vp, vp, vp, f32p,
+                                   vp, ctypes.c_size_t, vp]
+    lib.dsa_bwd_varlen.restype = ctypes.c_int
     lib.dsa_topk_compact.argtypes = [prob, i32p, i32p, i32p, i32p, vp]
     lib.dsa_topk_compact.restype = ctypes.c_int
     lib.dsa_device_status.argtypes = [vp]
@@ -145,13 +156,27 @@ def _need_residual_room(out, T, H):
                          "bf16 buffer (e.g. the `out` returned by fwd(..., delta_residual=True))")
 
 
+def _varlen(varlen, T, S_kv):
+    """(cu_seqlens_q, cu_seqlens_kv) device int32 tensors -> a Varlen struct."""
+    cu_q, cu_kv = varlen
+    B = cu_q.numel() - 1
+    if B < 1 or cu_kv.numel() != B + 1:
+        raise ValueError("varlen needs cu_seqlens_q and cu_seqlens_kv of B + 1 >= 2 entries")
+    for x, n in ((cu_q, "cu_seqlens_q"), (cu_kv, "cu_seqlens_kv")):
+        if x.dtype != torch.int32 or not x.is_cuda or not x.is_contiguous():
+            raise ValueError(f"{n}: contiguous int32 device tensor expected")
+    return Varlen(B, cu_q.data_ptr(), cu_kv.data_ptr())
+
+
 def fwd(q, kv, topk_idxs, topk_length=None, sink=None, scale=None, out=None, lse=None,
-        stream=None, delta_residual=False):
+        stream=None, delta_residual=False, varlen=None):
     """Sparse MLA forward.  Returns (out bf16 [T,H,512], lse fp32 [T,H]).
 
     With ``delta_residual`` the output is the first half of a [2,T,H,512]
     buffer whose second half holds the rounding residual that the backward
-    uses for an exact delta (DSA_FLAG_DELTA_RESIDUAL)."""
+    uses for an exact delta (DSA_FLAG_DELTA_RESIDUAL).  ``varlen`` =
+    (cu_seqlens_q, cu_seqlens_kv) selects dsa_fwd_varlen: packed sequences
+    whose indices count from their own first KV row."""
     prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale,
                                           FLAG_DELTA_RESIDUAL if delta_residual else 0)
     _need(q, "q", torch.bfloat16, (T, H, 576))
@@ -172,6 +197,13 @@ def fwd(q, kv, topk_idxs, topk_length=None, sink=None, scale=None, out=None, lse
         lse = torch.empty(T, H, dtype=torch.float32, device=q.device)
     _need(out, "out", torch.bfloat16, (T, H, 512))
     _need(lse, "lse", torch.float32, (T, H))
+    if varlen is not None:
+        vl = _varlen(varlen, T, S_kv)
+        _check(library().dsa_fwd_varlen(ctypes.byref(prob), ctypes.byref(vl), _ptr(q), _ptr(kv),
+                                        _ptr(topk_idxs), _ptr(topk_length), _ptr(sink), _ptr(out),
+                                        _ptr(lse), _stream(stream)),
+               "dsa_fwd_varlen")
+        return out, lse
     _check(library().dsa_fwd(ctypes.byref(prob), _ptr(q), _ptr(kv), _ptr(topk_idxs),
                              _ptr(topk_length), _ptr(sink), _ptr(out), _ptr(lse), _stream(stream)),
            "dsa_fwd")
@@ -185,13 +217,15 @@ def bwd_workspace_bytes(T, H, S_kv, W, scale=1.0 / 24.0, deterministic=False) ->
 
 def bwd(q, kv, topk_idxs, topk_length, sink, out, lse, dout, scale=None, dq=None, dkv=None,
         dsink=None, workspace=None, stream=None, entry="dsa_bwd", delta_residual=False,
-        deterministic=False):
+        deterministic=False, varlen=None):
     """Sparse MLA backward.  Returns (dq bf16, dkv bf16, dsink fp32 or None).
 
     ``entry`` selects ``dsa_bwd`` (all stages) or one of ``BWD_STAGES``.
     ``delta_residual`` must match the forward call that produced ``out``.
     ``deterministic`` (DSA_FLAG_DETERMINISTIC) makes dkv bitwise reproducible;
-    a caller-provided workspace must then be sized with the same flag."""
+    a caller-provided workspace must then be sized with the same flag.
+    ``varlen`` = (cu_seqlens_q, cu_seqlens_kv) selects dsa_bwd_varlen (all
+    stages in one call)."""
     flags = (FLAG_DELTA_RESIDUAL if delta_residual else 0) | \
         (FLAG_DETERMINISTIC if deterministic else 0)
     prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale, flags)
@@ -219,6 +253,18 @@ def bwd(q, kv, topk_idxs, topk_length, sink, out, lse, dout, scale=None, dq=None
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     if entry != "dsa_bwd" and entry not in BWD_STAGES:
         raise ValueError(entry)
+    if varlen is not None:
+        if entry != "dsa_bwd":
+            raise ValueError("varlen runs all backward stages in one call")
+        vl = _varlen(varlen, T, S_kv)
+        _check(library().dsa_bwd_varlen(ctypes.byref(prob), ctypes.byref(vl), _ptr(q), _ptr(kv),
+                                        _ptr(topk_idxs), _ptr(topk_length), _ptr(sink), _ptr(out),
+                                        _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv), _ptr(dsink),
+                                        _ptr(workspace),
+                                        ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                        _stream(stream)),
+               "dsa_bwd_varlen")
+        return dq, dkv, dsink
     _check(getattr(library(), entry)(ctypes.byref(prob), _ptr(q), _ptr(kv), _ptr(topk_idxs),
                              _ptr(topk_length), _ptr(sink), _ptr(out), _ptr(lse), _ptr(dout),
                              _ptr(dq), _ptr(dkv), _ptr(dsink), _ptr(workspace),

@@ -54,6 +54,9 @@ class Workload:
     dout: torch.Tensor         # [T, H, 512] bf16
     scale: float
     meta: dict = field(default_factory=dict)
+    # A varlen batch: int32 [B + 1] token and KV-row offsets, else None.
+    cu_seqlens_q: Optional[torch.Tensor] = None
+    cu_seqlens_kv: Optional[torch.Tensor] = None
 
     @property
     def T(self) -> int:
@@ -76,7 +79,8 @@ class Workload:
             return None if x is None else x.to(device)
         return Workload(self.name, mv(self.q), mv(self.kv), mv(self.topk_idxs),
                         mv(self.topk_length), mv(self.sink), mv(self.dout),
-                        self.scale, dict(self.meta))
+                        self.scale, dict(self.meta), mv(self.cu_seqlens_q),
+                        mv(self.cu_seqlens_kv))
 
 
 def _randn_bf16(gen: torch.Generator, shape, shift: float = 0.0) -> torch.Tensor:
@@ -159,6 +163,42 @@ def dsv4(T: int, H: int, topk: int, compact: bool, seed: int, name: str,
                     sink, dout, 1.0 / math.sqrt(D_QK),
                     {"T": T, "H": H, "S_kv": S_kv, "W": 128 + topk, "topk": topk,
                      "compact": compact, "seed": seed})
+
+
+def varlen(lengths, H: int, topk: int, compact: bool, seed: int) -> Workload:
+    """A varlen batch of DeepSeek-V4-like sequences, packed.
+
+    Sequence b has T_b = lengths[b] tokens and T_b + T_b // 4 KV rows, laid out
+    as in ``dsv4`` with indices counted from its own first KV row.  All rows
+    are padded to the same width 128 + topk.  A length of 0 gives an empty
+    sequence (no tokens, no KV rows).
+    """
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    W = 128 + topk
+    idx_parts, len_parts, cu_q, cu_kv = [], [], [0], [0]
+    for T_b in lengths:
+        S_b = T_b + T_b // 4
+        if T_b > 0:
+            idx = _window_and_compressed(T_b, topk, rng)
+            if compact:
+                idx, ln = _compact(idx, S_b)
+                len_parts.append(ln)
+            idx_parts.append(idx)
+        cu_q.append(cu_q[-1] + T_b)
+        cu_kv.append(cu_kv[-1] + S_b)
+    T, S_kv = cu_q[-1], cu_kv[-1]
+    idx = np.concatenate(idx_parts, axis=0) if idx_parts else np.zeros((0, W), np.int64)
+    q = _randn_bf16(gen, (T, H, D_QK))
+    kv = _randn_bf16(gen, (S_kv, D_QK))
+    dout = _randn_bf16(gen, (T, H, D_V))
+    sink = torch.randn(H, generator=gen, dtype=torch.float32)
+    length = torch.from_numpy(np.concatenate(len_parts).astype(np.int32)) if compact else None
+    return Workload(f"varlen{list(lengths)}", q, kv, torch.from_numpy(idx.astype(np.int32)),
+                    length, sink, dout, 1.0 / math.sqrt(D_QK),
+                    {"lengths": list(lengths), "H": H, "topk": topk, "compact": compact,
+                     "seed": seed},
+                    torch.tensor(cu_q, dtype=torch.int32), torch.tensor(cu_kv, dtype=torch.int32))
 
 
 def tiny(seed: int = 1000) -> Workload:

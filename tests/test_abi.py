@@ -92,3 +92,21 @@ def test_backward_argument_checks(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         dsa.library(str(tmp_path / "missing.so"))
+
+
+def test_varlen_descriptor_checks(lib):
+    """dsa_fwd_varlen / dsa_bwd_varlen reject a bad batch descriptor before
+    any launch (the offsets themselves are never read on the host)."""
+    p = P(T=4, H=16, S_kv=8, W=4)
+    fake = ctypes.c_void_p(1 << 20)
+    a4 = ctypes.c_void_p(1 << 21)
+    assert lib.dsa_fwd_varlen(ctypes.byref(p), None, fake, fake, fake, None, None, fake, fake,
+                              None) == 1
+    for v, code in [(dsa.Varlen(0, a4.value, a4.value), 1), (dsa.Varlen(2, None, a4.value), 1),
+                    (dsa.Varlen(2, a4.value, None), 1),
+                    (dsa.Varlen(2, (1 << 21) + 2, a4.value), 3)]:
+        assert lib.dsa_fwd_varlen(ctypes.byref(p), ctypes.byref(v), fake, fake, fake, None, None,
+                                  fake, fake, None) == code
+        assert lib.dsa_bwd_varlen(ctypes.byref(p), ctypes.byref(v), fake, fake, fake, None, None,
+                                  fake, fake, fake, fake, fake, None, fake, ctypes.c_size_t(0),
+                                  None) == code
