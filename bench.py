@@ -327,6 +327,9 @@ def run_ours(args, rank, world, local):
     bwd_det_ms = d0.elapsed_time(d1) / args.steps
     del ws_det
 
+    varlen_leg = run_varlen_leg(args, dev, stream)
+    d512_leg = run_d512_leg(args, dev, stream)
+
     # End to end through the public API: pinned host inputs -> device, fwd + bwd,
     # outputs -> pinned host, every step.
     e2e = None
@@ -356,6 +359,8 @@ def run_ours(args, rank, world, local):
                            "bwd_finalize (k_bwd_dkv + cast + d_sink)": fin_ms},
             "bwd_ms": pre_ms + main_ms + fin_ms,
             "bwd_deterministic_ms": bwd_det_ms,
+            "varlen": varlen_leg,
+            "d512": d512_leg,
             "fwd_tflops": fwd_tflops,
             "bwd_finalize_tflops": bwd_dkv_flops / (fin_ms * 1e-3) / 1e12,
             "roofline": {"kernel": "k_bwd_dq", "bound": "tensor", "achieved": main_tflops,
@@ -368,6 +373,92 @@ def run_ours(args, rank, world, local):
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+def run_varlen_leg(args, dev, stream):
+    """fwd + bwd through dsa_fwd_varlen / dsa_bwd_varlen on four packed
+    2048-token sequences (the same 8192 tokens as the headline workload, each
+    sequence with its own window and compressed rows)."""
+    from sparse_top_attention_gb300 import dsa
+    from sparse_top_attention_gb300 import workloads as WL
+    lengths = [2048] * 4
+    w = WL.varlen(lengths, H=WORKLOAD["H"], topk=WORKLOAD["topk"], compact=False, seed=1006,
+                  value_device=str(dev))
+    sum_k = float(sum(WL.valid_slot_count_formula(n, WORKLOAD["topk"]).sum() for n in lengths))
+    flops = 3.5 * FWD_FLOPS_PER_SLOT_HEAD * w.H * sum_k
+    vl = (w.cu_seqlens_q, w.cu_seqlens_kv)
+    out = torch.empty(w.T, w.H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.T, w.H, dtype=torch.float32, device=dev)
+    dq = torch.empty(w.T, w.H, 576, dtype=torch.bfloat16, device=dev)
+    dkv = torch.empty(w.S_kv, 576, dtype=torch.bfloat16, device=dev)
+    dsink = torch.empty(w.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(dsa.bwd_workspace_bytes(w.T, w.H, w.S_kv, w.W), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        dsa.fwd(w.q, w.kv, w.topk_idxs, None, w.sink, w.scale, out=out, lse=lse, varlen=vl)
+        dsa.bwd(w.q, w.kv, w.topk_idxs, None, w.sink, out, lse, w.dout, w.scale, dq=dq, dkv=dkv,
+                dsink=dsink, workspace=ws, varlen=vl)
+
+    for _ in range(args.warmup):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert dsa.device_status() == 0
+    ms = e0.elapsed_time(e1) / args.steps
+    return {"workload": "4 packed sequences x 2048 tokens, H=128, window 128 + top-k 512",
+            "valid_slots": int(sum_k), "ms_per_step": ms,
+            "tflops": flops / (ms * 1e-3) / 1e12}
+
+
+def run_d512_leg(args, dev, stream):
+    """The same layout with D_qk = D_v = 512 (no rope part), the row width of
+    the DeepSeek-V4 performance table on the flash-attention page: fwd and
+    bwd timed separately, FLOPs by valid slots (2 * H * (512 + 512) each)."""
+    from sparse_top_attention_gb300 import dsa
+    from sparse_top_attention_gb300 import workloads as WL
+    w = WL.dsv4(T=WORKLOAD["T"], H=WORKLOAD["H"], topk=WORKLOAD["topk"], compact=False,
+                seed=1007, name="flash_t8k_d512", value_device=str(dev), d_qk=512)
+    sum_k = float(WL.valid_slot_count_formula(w.T, WORKLOAD["topk"]).sum())
+    fwd_flops = 2 * (512 + 512) * w.H * sum_k
+    out = torch.empty(w.T, w.H, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.T, w.H, dtype=torch.float32, device=dev)
+    dq = torch.empty(w.T, w.H, 512, dtype=torch.bfloat16, device=dev)
+    dkv = torch.empty(w.S_kv, 512, dtype=torch.bfloat16, device=dev)
+    dsink = torch.empty(w.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(dsa.bwd_workspace_bytes(w.T, w.H, w.S_kv, w.W, d_qk=512),
+                     dtype=torch.uint8, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+
+    def step(e=None):
+        if e:
+            e[0].record(stream)
+        dsa.fwd(w.q, w.kv, w.topk_idxs, None, w.sink, w.scale, out=out, lse=lse)
+        if e:
+            e[1].record(stream)
+        dsa.bwd(w.q, w.kv, w.topk_idxs, None, w.sink, out, lse, w.dout, w.scale, dq=dq, dkv=dkv,
+                dsink=dsink, workspace=ws)
+        if e:
+            e[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for e in ev:
+        step(e)
+    torch.cuda.synchronize()
+    assert dsa.device_status() == 0
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    return {"workload": "flash layout T=8192 H=128, window 128 + top-k 512, D_qk=D_v=512",
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
+            "bwd_tflops": 2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12}
 
 
 def run_e2e(args, w, dev, stream, step_flops, world):

@@ -9,12 +9,14 @@
  *       attention-sink boundary failures", Why item 2.
  *     - cuDNN frontend "DSA bwd SM100 fix dropped dKV gradients when topk
  *       width > total_S_kv": a column position >= S_kv is not invalid.
- *   s_j = scale * q[t,h,:] . kv[idx_j,:]  over all 576 columns.
+ *   s_j = scale * q[t,h,:] . kv[idx_j,:]  over all D = d_qk columns.
  *   lse[t,h] = log sum_j exp(s_j)  (natural log; the sink is not included).
  *   out[t,h,:] = sum_j exp(s_j) / (sum_j exp(s_j) + exp(sink[h])) * kv[idx_j, 0:512]
  * Every head uses the same KV tensor, whose first 512 columns are V
  * (flash-attention "[CuTe, SM100] Support 1..128 Q heads in sparse MLA via
- * in-kernel TMA padding", Agent Notes).  The backward takes the loss
+ * in-kernel TMA padding", Agent Notes).  Rows are D = d_qk = 576 columns
+ * (512 V + 64 rope), or 512 with no rope part, the width that page's
+ * section "Performance at DeepSeek-V4 shapes" measures.  The backward takes the loss
  * sum(dout * out) and returns dq, dkv (summed over every token and head
  * that gathered a row) and d_sink (cuDNN page above, "Not addressed" and
  * Testing).
@@ -22,8 +24,10 @@
  * Conventions, for every entry point:
  *  - Tensors are dense and row-major.  Device pointers are 16-byte aligned,
  *    else DSA_ERR_ALIGNMENT.
- *  - The caller owns every buffer.  The library allocates nothing and keeps
- *    no host state; the entry points are thread-safe.
+ *  - The caller owns every buffer.  The library never allocates device
+ *    memory.  Its only host state is set up on first use: each kernel's
+ *    shared-memory limit, and the device address of dsa_bwd_no_alloc's
+ *    array.  Make a first call before any stream capture.
  *  - All work is queued on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream) and the calls return before it finishes.
  *  - Argument and shape errors are returned before anything is launched.
@@ -59,9 +63,9 @@ typedef enum {
 typedef struct {
   int32_t T;       /* query tokens, >= 0                                   */
   int32_t H;       /* query heads, 1..128                                  */
-  int32_t S_kv;    /* KV rows, 1..3728270 (576 * S_kv < 2^31)              */
+  int32_t S_kv;    /* KV rows, >= 1, with d_qk * S_kv < 2^31               */
   int32_t W;       /* index slots per token, >= 1                         */
-  int32_t d_qk;    /* q/kv row width; must be 576                          */
+  int32_t d_qk;    /* q/kv row width D: 576 (512 V + 64 rope) or 512 (V)  */
   int32_t d_v;     /* V width (leading columns of kv); must be 512         */
   float scale;     /* softmax scale applied to q.kv (e.g. 1/sqrt(576))     */
   uint32_t flags;  /* OR of DSA_FLAG_DELTA_RESIDUAL, DSA_FLAG_DETERMINISTIC  */
@@ -101,8 +105,8 @@ typedef struct {
 
 /*
  * Forward.  Shapes and types (all device pointers):
- *   q            bf16  [T, H, 576]
- *   kv           bf16  [S_kv, 576]
+ *   q            bf16  [T, H, D]     (D = d_qk: 576, or 512 with no rope part)
+ *   kv           bf16  [S_kv, D]
  *   topk_idxs    int32 [T, W]
  *   topk_length  int32 [T], or NULL for the non-compact encoding
  *                (-1 marks unused slots)
@@ -119,7 +123,7 @@ dsa_status_t dsa_fwd(const dsa_problem_t* problem, const void* q, const void* kv
 /*
  * Bytes of device workspace that dsa_bwd needs for `problem`.  Returns 0 on
  * an invalid problem.  The workspace holds:
- *   - the dkv accumulator             [S_kv, 576], fp32 (int64 with
+ *   - the dkv accumulator             [S_kv, D], fp32 (int64 with
  *                                     DSA_FLAG_DETERMINISTIC);
  *   - the compacted index lists       [T, W] and their counts [T];
  *   - per-(t,h) fp32 rows: lse*log2(e), sigma(lse - sink), delta and the
@@ -139,8 +143,8 @@ size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem);
  *   lse    fp32 [T, H]       the forward's lse
  *   dout   bf16 [T, H, 512]
  * Outputs, all overwritten, never accumulated:
- *   dq     bf16 [T, H, 576]
- *   dkv    bf16 [S_kv, 576]  rows that no valid slot names are written as 0
+ *   dq     bf16 [T, H, D]
+ *   dkv    bf16 [S_kv, D]    rows that no valid slot names are written as 0
  *   dsink  fp32 [H]          must be NULL exactly when sink is NULL
  * workspace: device memory of at least dsa_bwd_workspace_bytes(problem)
  * bytes, 256-byte aligned.  It is overwritten.

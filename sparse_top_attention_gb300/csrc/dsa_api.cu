@@ -19,17 +19,19 @@ dsa_status_t check_problem(const dsa_problem_t* p) {
   if ((p->flags & ~(DSA_FLAG_DELTA_RESIDUAL | DSA_FLAG_DETERMINISTIC)) != 0u)
     return DSA_ERR_INVALID_ARG;
   if (!(p->scale == p->scale)) return DSA_ERR_INVALID_ARG;  // NaN scale
-  if (p->d_qk != 576 || p->d_v != 512) return DSA_ERR_UNSUPPORTED;
+  if ((p->d_qk != 576 && p->d_qk != 512) || p->d_v != 512) return DSA_ERR_UNSUPPORTED;
   if (p->H > 128) return DSA_ERR_UNSUPPORTED;
   // The backward addresses accumulator rows with 32-bit element offsets.
-  if (static_cast<int64_t>(p->S_kv) * 576 > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(p->S_kv) * p->d_qk > INT32_MAX) return DSA_ERR_UNSUPPORTED;
   return DSA_OK;
 }
 
 dsa::Problem to_internal(const dsa_problem_t* p) {
-  return dsa::Problem{p->T, p->H, p->S_kv, p->W, p->scale,
-                      (p->flags & DSA_FLAG_DELTA_RESIDUAL) != 0u,
-                      (p->flags & DSA_FLAG_DETERMINISTIC) != 0u};
+  dsa::Problem q{p->T, p->H, p->S_kv, p->W, p->scale,
+                 (p->flags & DSA_FLAG_DELTA_RESIDUAL) != 0u,
+                 (p->flags & DSA_FLAG_DETERMINISTIC) != 0u};
+  q.d_qk = p->d_qk;
+  return q;
 }
 
 dsa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }

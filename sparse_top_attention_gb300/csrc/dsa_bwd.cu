@@ -56,7 +56,7 @@ BwdWorkspace bwd_workspace_layout(const Problem& p) {
   BwdWorkspace w{};
   size_t off = 0;
   const size_t TH = static_cast<size_t>(p.T) * p.H;
-  w.dkv_acc = off; off = up(off + static_cast<size_t>(p.S_kv) * kDqk * (p.deterministic ? 8 : 4));
+  w.dkv_acc = off; off = up(off + static_cast<size_t>(p.S_kv) * p.d_qk * (p.deterministic ? 8 : 4));
   w.idxc = off;    off = up(off + static_cast<size_t>(p.T) * p.W * 4);
   w.count = off;   off = up(off + static_cast<size_t>(p.T) * 4);
   w.lse2 = off;    off = up(off + TH * 4);
@@ -158,16 +158,7 @@ constexpr int kThreads = 256;
 constexpr int kProducers = 96;           // warps 5-7
 constexpr int kKVChunk = kBlk * 128;     // 16 KB
 constexpr int kHChunk = kHG * 128;       // 4 KB: 64 columns of 32 head rows
-// smem position p of the gathered block holds d-chunk x(p): p = 0 the rope
-// columns 512..575 (reused for the P tile once the rope part of dQ is done),
-// p = 1..8 the V chunks 0..7.  Blocks are gathered and consumed in the order
-// p = 1..8, 0 because position 0 is released last.
-constexpr int kOffKV = 0;
 constexpr int kQdO = 2 * kHChunk;                   // Q chunk x, then dO chunk x
-constexpr int kOffQD = kOffKV + kChunks * kKVChunk;  // 8 (Q, dO) pairs, then the Q rope chunk
-constexpr int kOffdS = kOffQD + 8 * kQdO + kHChunk;  // 2 sub-tiles of 64 slots
-constexpr int kOffMisc = kOffdS + 2 * kHChunk;
-constexpr int kOffP = kOffKV;                       // P tile in position 0
 
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColdP = 32, kColdQ = 64;
@@ -181,9 +172,26 @@ struct Misc {
   int abort_flag;
 };
 
-constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffQD % 1024 == 0 && kOffdS % 1024 == 0, "alignment");
+// Shared-memory layout for rows of kD columns (576 = 512 V + 64 rope, or 512).
+// With a rope chunk, position p of the gathered block holds d-chunk x(p):
+// p = 0 the rope columns 512..575 (reused for the P tile once the rope part
+// of dQ is done), p = 1..8 the V chunks 0..7; blocks are gathered and
+// consumed in the order p = 1..8, 0 because position 0 is released last.
+// Without one, position p holds V chunk p and P has a tile of its own.
+template <int kD>
+struct DqLayout {
+  static constexpr int kCh = kD / 64;
+  static constexpr bool kRope = kCh > 8;
+  static constexpr int kDT = (kD + 127) / 128;   // 128-row d tiles of dQ^T
+  static constexpr int kOffKV = 0;
+  static constexpr int kOffQD = kOffKV + kCh * kKVChunk;  // 8 (Q, dO) pairs, then Q rope
+  static constexpr int kOffdS = kOffQD + 8 * kQdO + (kRope ? kHChunk : 0);  // 2 sub-tiles
+  static constexpr int kOffP = kRope ? kOffKV : kOffdS + 2 * kHChunk;
+  static constexpr int kOffMisc = kRope ? kOffdS + 2 * kHChunk : kOffP + 2 * kHChunk;
+  static constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kOffQD % 1024 == 0 && kOffdS % 1024 == 0 && kOffP % 1024 == 0, "alignment");
+};
 
 template <unsigned int* kErr>
 __device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
@@ -196,9 +204,15 @@ __device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ int dchunk_of_pos(int pos) { return pos == 0 ? 8 : pos - 1; }
+template <bool kRope>
+__device__ __forceinline__ int dchunk_of_pos(int pos) {
+  return kRope ? (pos == 0 ? 8 : pos - 1) : pos;
+}
 // Gather / S-GEMM order of the shared positions: V chunks first, rope last.
-__device__ __forceinline__ int pos_of_step(int i) { return i == kChunks - 1 ? 0 : i + 1; }
+template <bool kRope>
+__device__ __forceinline__ int pos_of_step(int i) {
+  return kRope ? (i == kChunks - 1 ? 0 : i + 1) : i;
+}
 
 // Byte offset of element (head row h, slot) in a [32 rows x 128 slots] bf16
 // tile kept as two 128B-swizzled sub-tiles of 64 slots: the layout of dS' and
@@ -209,6 +223,7 @@ __device__ __forceinline__ uint32_t hs_tile_off(uint32_t h, uint32_t slot) {
   return (slot >> 6) * kHChunk + h * 128u + ((((col >> 3) ^ (h & 7u)) << 4) | ((col & 7u) << 1));
 }
 
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
 k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
          const __grid_constant__ CUtensorMap tm_sp, const __nv_bfloat16* __restrict__ kv,
@@ -216,6 +231,10 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
          const float* __restrict__ lse2_g, const float* __restrict__ gate_g,
          const float* __restrict__ delta_g, __nv_bfloat16* __restrict__ dq, int T, int H, int W,
          float scale, int G, int box_heads, int nbmax) {
+  using L = DqLayout<kD>;
+  constexpr int kCh = L::kCh, kDT = L::kDT, kOffKV = L::kOffKV, kOffQD = L::kOffQD,
+                kOffdS = L::kOffdS, kOffP = L::kOffP, kOffMisc = L::kOffMisc;
+  constexpr bool kRope = L::kRope;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
@@ -231,9 +250,9 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   const int Kt = count[t];
 
   if (Kt == 0) {  // empty row: dq = 0, nothing for dkv
-    for (int v = tid; v < nh * (kDqk / 8); v += kThreads) {
-      const int h = v / (kDqk / 8), c = v - h * (kDqk / 8);
-      *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kDqk + c * 8) =
+    for (int v = tid; v < nh * (kD / 8); v += kThreads) {
+      const int h = v / (kD / 8), c = v - h * (kD / 8);
+      *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kD + c * 8) =
           make_uint4(0, 0, 0, 0);
     }
     return;
@@ -242,7 +261,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   const int32_t* rows = idxc + static_cast<size_t>(t) * W;
 
   if (tid == 0) {
-    for (int c = 0; c < kChunks; ++c) {
+    for (int c = 0; c < kCh; ++c) {
       mbar_init(smem_u32(&m.kv_full[c]), kProducers);
       mbar_init(smem_u32(&m.kv_free[c]), 1);
     }
@@ -265,12 +284,12 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     m.delta[tid] = real ? delta_g[r] : 0.f;
   }
   // Q / dO tile rows the TMA box does not cover (only when H < 32) are zero.
-  for (int i = tid; i < (kChunks + 8) * (kHG - box_heads) * 8; i += kThreads) {
+  for (int i = tid; i < (kCh + 8) * (kHG - box_heads) * 8; i += kThreads) {
     const int per = (kHG - box_heads) * 8;
     const int c = i / per, rem = i - c * per;
     const int row = box_heads + rem / 8, pc = rem & 7;
-    const uint32_t base = c < kChunks ? sbase + kOffQD + c * kQdO
-                                      : sbase + kOffQD + (c - kChunks) * kQdO + kHChunk;
+    const uint32_t base = c < kCh ? sbase + kOffQD + c * kQdO
+                                      : sbase + kOffQD + (c - kCh) * kQdO + kHChunk;
     asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(base + sw128_off(row, pc)), "r"(0u)
                  : "memory");
   }
@@ -290,8 +309,8 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     const int pw = warp - 5;
     if (tid == 160) {
       const uint64_t pol = l2_evict_first();
-      mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kChunks + 8) * box_heads * 128);
-      for (int c = 0; c < kChunks; ++c)
+      mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kCh + 8) * box_heads * 128);
+      for (int c = 0; c < kCh; ++c)
         tma_load_3d_hint(sbase + kOffQD + c * kQdO, &tm_q, c * 64, h0, t, smem_u32(&m.qd_full),
                          pol);
       for (int c = 0; c < 8; ++c)
@@ -311,14 +330,14 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         const int slot = b * kBlk + row;
         const bool ok = g < kBlk / 4 && slot < Kt;
         const int r = ok ? rows[slot] : 0;
-        src[k] = kv + static_cast<size_t>(r) * kDqk + pc * 8;
+        src[k] = kv + static_cast<size_t>(r) * kD + pc * 8;
         dst[k] = sw128_off(row & (kBlk - 1), pc);
         nbytes[k] = ok ? 16u : 0u;
       }
-      for (int i = 0; i < kChunks; ++i) {
-        const int pos = pos_of_step(i);
+      for (int i = 0; i < kCh; ++i) {
+        const int pos = pos_of_step<kRope>(i);
         if (b > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (b - 1) & 1, fs, 1);
-        const int x = dchunk_of_pos(pos);
+        const int x = dchunk_of_pos<kRope>(pos);
 #pragma unroll
         for (int k = 0; k < kRowGroups; ++k)
           if (pw + 3 * k < kBlk / 4)
@@ -336,12 +355,12 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       const uint32_t idQ = idesc_bf16(128, kHG, true, false);      // dQ^T: A MN-major, B K-major
       mbar_wait(smem_u32(&m.qd_full), 0, fs, 2);
       for (int b = 0; b < nblk; ++b) {
-        for (int i = 0; i < kChunks; ++i) {
-          const int pos = pos_of_step(i);
+        for (int i = 0; i < kCh; ++i) {
+          const int pos = pos_of_step<kRope>(i);
           mbar_wait(smem_u32(&m.kv_full[pos]), b & 1, fs, 3);
           fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
           tc_fence_after();
-          const int x = dchunk_of_pos(pos);
+          const int x = dchunk_of_pos<kRope>(pos);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t a = sdesc_sw128(sbase + kOffKV + pos * kKVChunk + k * 32, 16, 1024);
@@ -356,9 +375,9 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         tc_fence_after();
         // dQ^T chunks: rope first (its second 64-row atom reads V chunk 0 as
         // filler rows that are never stored), then d rows 0..511.
-        for (int jj = 0; jj < 5; ++jj) {
-          const int j = (jj == 0) ? 4 : jj - 1;
-          const int pos0 = (j == 4) ? 0 : 1 + 2 * j;
+        for (int jj = 0; jj < kDT; ++jj) {
+          const int j = kRope ? ((jj == 0) ? 4 : jj - 1) : jj;
+          const int pos0 = (j == 4) ? 0 : (kRope ? 1 + 2 * j : 2 * j);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t a =
@@ -413,8 +432,9 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&m.ds_full));
-      // P goes into position 0 once the rope part of dQ has read the rope rows.
-      mbar_wait(smem_u32(&m.rope_done), b & 1, fs, 9);
+      // With a rope chunk, P goes into position 0 once the rope part of dQ has
+      // read the rope rows.
+      if constexpr (kRope) mbar_wait(smem_u32(&m.rope_done), b & 1, fs, 9);
 #pragma unroll
       for (int h = 0; h < kHG; ++h) {
         const __nv_bfloat16 v = __float2bfloat16_rn(pv[h]);
@@ -434,28 +454,31 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         }
         bulk_commit();
         bulk_wait_read();
-        mbar_arrive(smem_u32(&m.kv_free[0]));  // position 0 may take the next rope rows
+        if constexpr (kRope) mbar_arrive(smem_u32(&m.kv_free[0]));  // position 0 may take the next rope rows
       }
     }
 
     // dQ^T -> dq (bf16), staged through shared memory for one bulk store.
+    // With a rope chunk the staging area overlaps the last P tile: thread 0
+    // reaches this barrier only after that tile's store has been read out.
+    named_bar_sync(1, 128);
     mbar_wait(smem_u32(&m.dq_done), 0, fs, 10);
     tc_fence_after();
-    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV);  // [32][576]
-    for (int j = 0; j < 5; ++j) {
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV);  // [32][kD]
+    for (int j = 0; j < kDT; ++j) {
       uint32_t v[32];
       tmem_ld32_sync(tmem + lane_base + kColdQ + j * kHG, v);
       const int d = j * 128 + tid;
-      if (d < kDqk) {
+      if (d < kD) {
 #pragma unroll
-        for (int h = 0; h < kHG; ++h) stage[h * kDqk + d] = __float2bfloat16_rn(__uint_as_float(v[h]));
+        for (int h = 0; h < kHG; ++h) stage[h * kD + d] = __float2bfloat16_rn(__uint_as_float(v[h]));
       }
     }
     fence_proxy_async_smem();
     named_bar_sync(1, 128);
     if (tid == 0) {  // dq rows (t, h0..h0+nh) are contiguous
-      bulk_store_hint(dq + (static_cast<size_t>(t) * H + h0) * kDqk, smem_u32(stage),
-                      nh * kDqk * 2, l2_evict_first());
+      bulk_store_hint(dq + (static_cast<size_t>(t) * H + h0) * kD, smem_u32(stage),
+                      nh * kD * 2, l2_evict_first());
       bulk_commit();
       bulk_wait_read();
     }
@@ -500,7 +523,7 @@ static_assert(kOffA % 1024 == 0, "alignment");
 
 // kDet: the accumulator is int64 in units of 2^-32 and the adds are integer
 // adds, so the sum does not depend on their order (bitwise reproducible).
-template <bool kDet>
+template <bool kDet, int kD>
 __global__ void __launch_bounds__(dkv::kThreads, 1)
 k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUtensorMap tm_doa,
           const __grid_constant__ CUtensorMap tm_spb, const int32_t* __restrict__ idxc,
@@ -512,6 +535,7 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
   using dkv::kOffB;
   using dkv::kOffA;
   using dkv::kAStage;
+  constexpr int kNT = (kD + 127) / 128;  // 128-row d tiles (the last may be a 64-row rope tile)
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x;
@@ -573,8 +597,8 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         const uint64_t pol = l2_evict_first();
         tma_load_2d_hint(sbase + kOffB, &tm_spb, 0, row0, smem_u32(&m.b_full), pol);
         tma_load_2d_hint(sbase + kOffB + b_half, &tm_spb, 64, row0, smem_u32(&m.b_full), pol);
-        for (int n = 0; n < 5; ++n) {
-          const int u = b * 5 + n, st = u & 1, use = u >> 1;
+        for (int n = 0; n < kNT; ++n) {
+          const int u = b * kNT + n, st = u & 1, use = u >> 1;
           if (use > 0) mbar_wait(smem_u32(&m.a_empty[st]), (use - 1) & 1, fs, 21);
           const uint32_t base = sbase + kOffA + st * kAStage;
           const int nd = n < 4 ? 2 : 1;  // 64-d boxes in this chunk
@@ -595,8 +619,8 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
       const uint32_t id = idesc_bf16(128, kBlk, true, true);
       for (int b = 0; b < nblk; ++b) {
         mbar_wait(smem_u32(&m.b_full), b & 1, fs, 22);
-        for (int n = 0; n < 5; ++n) {
-          const int u = b * 5 + n, st = u & 1, use = u >> 1;
+        for (int n = 0; n < kNT; ++n) {
+          const int u = b * kNT + n, st = u & 1, use = u >> 1;
           mbar_wait(smem_u32(&m.a_full[st]), use & 1, fs, 23);
           if (use > 0) mbar_wait(smem_u32(&m.d_empty[st]), (use - 1) & 1, fs, 24);
           tc_fence_after();
@@ -638,9 +662,9 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
       const int nvalid = max(0, min(32, Kt - s0));
       // Lane s holds the accumulator offset of slot s0 + s; shuffles hand it
       // to the whole warp without a shared-memory round trip per add.
-      const uint32_t roff = lane < nvalid ? static_cast<uint32_t>(rows[s0 + lane]) * kDqk : 0u;
-      for (int n = 0; n < 5; ++n) {
-        const int u = b * 5 + n, st = u & 1, use = u >> 1;
+      const uint32_t roff = lane < nvalid ? static_cast<uint32_t>(rows[s0 + lane]) * kD : 0u;
+      for (int n = 0; n < kNT; ++n) {
+        const int u = b * kNT + n, st = u & 1, use = u >> 1;
         mbar_wait(smem_u32(&m.d_full[st]), use & 1, fs, 25);
         tc_fence_after();
         uint32_t v[32];
@@ -648,7 +672,7 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         tc_fence_before();
         mbar_arrive(smem_u32(&m.d_empty[st]));
         const int d = n * 128 + sp * 32 + lane;
-        if (n < 4 || d < kDqk) {
+        if (n < 4 || d < kD) {
           if constexpr (kDet) {
             unsigned long long* dst = static_cast<unsigned long long*>(dkv_acc) + d;
 #pragma unroll
@@ -740,14 +764,18 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
                        cudaStream_t s, int stages) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<576>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DqLayout<576>::kSmemBytes);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_bwd_dkv<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dkv::kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_bwd_dkv<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               dkv::kSmemBytes);
+      e = cudaFuncSetAttribute(k_bwd_dq<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DqLayout<512>::kSmemBytes);
+    void (*dkv_kernels[])(CUtensorMap, CUtensorMap, CUtensorMap, const int32_t*, const int32_t*,
+                          void*, int, int, int, int, int, int) = {
+        k_bwd_dkv<false, 576>, k_bwd_dkv<true, 576>, k_bwd_dkv<false, 512>, k_bwd_dkv<true, 512>};
+    for (auto k : dkv_kernels)
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -760,7 +788,7 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
   float* gate = reinterpret_cast<float*>(base + L.gate);
   float* delta = reinterpret_cast<float*>(base + L.delta);
   float* dsink_t = reinterpret_cast<float*>(base + L.dsink_t);
-  const size_t acc_bytes = static_cast<size_t>(p.S_kv) * kDqk * (p.deterministic ? 8 : 4);
+  const size_t acc_bytes = static_cast<size_t>(p.S_kv) * p.d_qk * (p.deterministic ? 8 : 4);
   cudaError_t e = cudaSuccess;
   if (stages & kBwdPre) {
     e = cudaMemsetAsync(acc, 0, acc_bytes, s);
@@ -782,11 +810,13 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     const long long sp_rows = static_cast<long long>(p.T) * nbmax * 64 * G;
     CUtensorMap tm_q, tm_do, tm_sp_st;
     const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
-    e = make_head_tile_map(&tm_q, q, p.T, p.H, kDqk, box_heads);
+    e = make_head_tile_map(&tm_q, q, p.T, p.H, p.d_qk, box_heads);
     if (e == cudaSuccess) e = make_head_tile_map(&tm_do, dout, p.T, p.H, kDv, box_heads);
     if (e == cudaSuccess) e = make_matrix_map(&tm_sp_st, sp, sp_rows, kBlk, 32);
     if (e != cudaSuccess) return e;
-    k_bwd_dq<<<static_cast<unsigned>(static_cast<long long>(p.T) * G), kThreads, kSmemBytes, s>>>(
+    auto kern = p.d_qk == 512 ? k_bwd_dq<512> : k_bwd_dq<576>;
+    const int smem = p.d_qk == 512 ? DqLayout<512>::kSmemBytes : DqLayout<576>::kSmemBytes;
+    kern<<<static_cast<unsigned>(static_cast<long long>(p.T) * G), kThreads, smem, s>>>(
         tm_q, tm_do, tm_sp_st, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2, gate,
         delta, static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, box_heads, nbmax);
     e = cudaGetLastError();
@@ -799,18 +829,19 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     CUtensorMap tm_qa, tm_doa, tm_sp_ld;
     const int HP = 32 * G;
     const int box_all = p.H < HP ? p.H : HP;
-    e = make_head_tile_map(&tm_qa, q, p.T, p.H, kDqk, box_all);
+    e = make_head_tile_map(&tm_qa, q, p.T, p.H, p.d_qk, box_all);
     if (e == cudaSuccess) e = make_head_tile_map(&tm_doa, dout, p.T, p.H, kDv, box_all);
     if (e == cudaSuccess) e = make_matrix_map(&tm_sp_ld, sp, sp_rows, kBlk, 2 * HP);
     if (e != cudaSuccess) return e;
-    auto kern = p.deterministic ? k_bwd_dkv<true> : k_bwd_dkv<false>;
+    auto kern = p.d_qk == 512 ? (p.deterministic ? k_bwd_dkv<true, 512> : k_bwd_dkv<false, 512>)
+                              : (p.deterministic ? k_bwd_dkv<true, 576> : k_bwd_dkv<false, 576>);
     kern<<<static_cast<unsigned>(p.T), dkv::kThreads, dkv::kSmemBytes, s>>>(
         tm_qa, tm_doa, tm_sp_ld, idxc, count, acc, p.T, p.H, p.W, G, box_all, nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdFinal) {
-    const long long n8 = static_cast<long long>(p.S_kv) * kDqk / 8;
+    const long long n8 = static_cast<long long>(p.S_kv) * p.d_qk / 8;
     if (p.deterministic)
       k_dkv_cast_fixed<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
           static_cast<const long long*>(acc), static_cast<__nv_bfloat16*>(dkv), n8);

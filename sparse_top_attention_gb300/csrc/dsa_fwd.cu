@@ -44,11 +44,6 @@ constexpr int kQIssuer = 160;               // lane 0 of warp 5
 constexpr int kProducers = 96;              // warps 5-7
 constexpr int kQChunk = kHG * 128;           // one 64-column chunk of Q: 8 KB
 constexpr int kKVChunk = kBlk * 128;         // one 64-column chunk of 128 rows: 16 KB
-constexpr int kOffKV = 0;                    // chunks 0..7 = V (d 0..511), 8 = rope (d 512..575)
-constexpr int kOffQ = kOffKV + kChunks * kKVChunk;
-constexpr int kOffList = kOffQ + kChunks * kQChunk;
-constexpr int kOffMisc = kOffList + kMaxW * 4;
-constexpr int kOffP = kOffKV + 8 * kKVChunk;  // P^T reuses the rope chunk once S is done
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
@@ -67,9 +62,22 @@ struct Misc {
   int abort_flag;
 };
 
-constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+// Shared-memory layout for rows of kD columns (576 = 512 V + 64 rope, or 512).
+// Chunks 0..7 of the KV tile are V (d 0..511), chunk 8 the rope columns.
+template <int kD>
+struct FwdLayout {
+  static constexpr int kCh = kD / 64;         // 64-column chunks of a row
+  static constexpr bool kRope = kCh > 8;
+  static constexpr int kOffKV = 0;
+  static constexpr int kOffQ = kOffKV + kCh * kKVChunk;
+  static constexpr int kOffList = kOffQ + kCh * kQChunk;
+  // P^T reuses the rope chunk once S is done; without one it has its own tile.
+  static constexpr int kOffP = kRope ? kOffKV + 8 * kKVChunk : kOffList + kMaxW * 4;
+  static constexpr int kOffMisc = kRope ? kOffList + kMaxW * 4 : kOffP + kKVChunk;
+  static constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+};
 
 __device__ __forceinline__ float warp_max(float v) {
   float r;
@@ -89,12 +97,16 @@ __device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
   }
 }
 
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
            const float* __restrict__ sink, __nv_bfloat16* __restrict__ out,
            float* __restrict__ lse, const __nv_bfloat16* __restrict__ kv, int T, int H, int S_kv,
            int W, float scale, int G, int residual, int box_heads,
            const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv, int B) {
+  using L = FwdLayout<kD>;
+  constexpr int kCh = L::kCh, kOffKV = L::kOffKV, kOffQ = L::kOffQ, kOffList = L::kOffList,
+                kOffP = L::kOffP, kOffMisc = L::kOffMisc;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
@@ -110,7 +122,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
   const FailState fs{&g_err_fwd, &m.abort_flag};
 
   if (tid == 0) {
-    for (int c = 0; c < kChunks; ++c) {
+    for (int c = 0; c < kCh; ++c) {
       mbar_init(smem_u32(&m.kv_full[c]), kProducers);
       mbar_init(smem_u32(&m.kv_free[c]), 1);
     }
@@ -124,7 +136,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
   }
   if (tid < kHG) m.m_used[tid] = -INFINITY;
   // Q tile rows that the TMA box does not cover (only when H < 64) are zero.
-  for (int i = tid; i < kChunks * (kHG - box_heads) * 8; i += kThreads) {
+  for (int i = tid; i < kCh * (kHG - box_heads) * 8; i += kThreads) {
     const int per = (kHG - box_heads) * 8;
     const int c = i / per, rem = i - c * per;
     const int row = box_heads + rem / 8, pc = rem & 7;
@@ -139,9 +151,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
   // swizzle; heads past H inside the box are zero-filled by the TMA) loads
   // while the slots are decoded.
   if (tid == kQIssuer) {
-    mbar_arrive_expect_tx(smem_u32(&m.q_full), kChunks * box_heads * 128);
+    mbar_arrive_expect_tx(smem_u32(&m.q_full), kCh * box_heads * 128);
     const uint64_t pol = l2_evict_first();
-    for (int c = 0; c < kChunks; ++c)
+    for (int c = 0; c < kCh; ++c)
       tma_load_3d_hint(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t, smem_u32(&m.q_full),
                        pol);
   }
@@ -192,11 +204,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
         const int slot = b * kBlk + row;
         const bool ok = g < kBlk / 4 && slot < Kt;
         const int r = ok ? list[slot] : 0;
-        src[k] = kv + static_cast<size_t>(r) * kDqk + pc * 8;
+        src[k] = kv + static_cast<size_t>(r) * kD + pc * 8;
         dst[k] = sw128_off(row & (kBlk - 1), pc);
         nbytes[k] = ok ? 16u : 0u;
       }
-      for (int c = 0; c < kChunks; ++c) {
+      for (int c = 0; c < kCh; ++c) {
         if (b > 0) mbar_wait(smem_u32(&m.kv_free[c]), (b - 1) & 1, fs, 1);
 #pragma unroll
         for (int k = 0; k < kRowGroups; ++k)
@@ -215,7 +227,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
       const uint32_t tS = tmem + kColS, tO = tmem + kColO;
       mbar_wait(smem_u32(&m.q_full), 0, fs, 2);
       for (int b = 0; b < nblk; ++b) {
-        for (int c = 0; c < kChunks; ++c) {
+        for (int c = 0; c < kCh; ++c) {
           mbar_wait(smem_u32(&m.kv_full[c]), b & 1, fs, 3);
           fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
           tc_fence_after();
@@ -240,7 +252,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
           umma_commit(smem_u32(&m.kv_free[2 * j]));
           umma_commit(smem_u32(&m.kv_free[2 * j + 1]));
         }
-        umma_commit(smem_u32(&m.kv_free[8]));
+        if constexpr (L::kRope) umma_commit(smem_u32(&m.kv_free[8]));
         umma_commit(smem_u32(&m.o_done));
       }
       umma_commit(smem_u32(&m.mma_done));
@@ -397,8 +409,12 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const in
                        cudaStream_t s) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<576>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         FwdLayout<576>::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fwd_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               FwdLayout<512>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -407,9 +423,11 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const in
   if (grid == 0) return cudaSuccess;
   CUtensorMap tm_q;
   const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
-  cudaError_t e = make_head_tile_map(&tm_q, q, p.T, p.H, kDqk, box_heads);
+  cudaError_t e = make_head_tile_map(&tm_q, q, p.T, p.H, p.d_qk, box_heads);
   if (e != cudaSuccess) return e;
-  fwd_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(
+  auto kern = p.d_qk == 512 ? fwd_kernel<512> : fwd_kernel<576>;
+  const int smem = p.d_qk == 512 ? FwdLayout<512>::kSmemBytes : FwdLayout<576>::kSmemBytes;
+  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(
       tm_q, idx, len, sink, static_cast<__nv_bfloat16*>(out), lse,
       static_cast<const __nv_bfloat16*>(kv), p.T, p.H, p.S_kv, p.W, p.scale, G,
       p.delta_residual ? 1 : 0, box_heads, p.cu_q, p.cu_kv, p.B);

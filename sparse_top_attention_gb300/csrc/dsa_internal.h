@@ -13,6 +13,7 @@ struct Problem {
   float scale;
   bool delta_residual;  // out holds [2, T, H, 512]: rounded output, then its residual
   bool deterministic;   // dkv summed as 64-bit fixed point (order-independent)
+  int d_qk = 576;        // q / kv row width: 576 (512 V + 64 rope) or 512 (V only)
   // Varlen batch (device arrays of B + 1 offsets), or nullptr for one sequence.
   const int32_t* cu_q = nullptr;
   const int32_t* cu_kv = nullptr;

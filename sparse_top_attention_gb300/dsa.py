@@ -119,8 +119,8 @@ def _check(code: int, what: str):
         raise DsaError(code, what)
 
 
-def make_problem(T, H, S_kv, W, scale, flags=0) -> Problem:
-    return Problem(int(T), int(H), int(S_kv), int(W), 576, 512, float(scale), int(flags))
+def make_problem(T, H, S_kv, W, scale, flags=0, d_qk=576) -> Problem:
+    return Problem(int(T), int(H), int(S_kv), int(W), int(d_qk), 512, float(scale), int(flags))
 
 
 def _need(x: torch.Tensor, name: str, dtype, shape=None):
@@ -137,12 +137,13 @@ def _need(x: torch.Tensor, name: str, dtype, shape=None):
 
 
 def _problem_from(q, kv, topk_idxs, scale, flags=0):
-    T, H, dq = q.shape
+    """The problem of these tensors; q's last dimension is d_qk (576 or 512)."""
+    T, H, d_qk = q.shape
     S_kv = kv.shape[0]
     W = topk_idxs.shape[1]
     if scale is None:
-        scale = 1.0 / math.sqrt(dq)
-    return make_problem(T, H, S_kv, W, scale, flags), (T, H, S_kv, W)
+        scale = 1.0 / math.sqrt(d_qk)
+    return make_problem(T, H, S_kv, W, scale, flags, d_qk), (T, H, S_kv, W)
 
 
 def _need_residual_room(out, T, H):
@@ -179,8 +180,9 @@ def fwd(q, kv, topk_idxs, topk_length=None, sink=None, scale=None, out=None, lse
     whose indices count from their own first KV row."""
     prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale,
                                           FLAG_DELTA_RESIDUAL if delta_residual else 0)
-    _need(q, "q", torch.bfloat16, (T, H, 576))
-    _need(kv, "kv", torch.bfloat16, (S_kv, 576))
+    D = prob.d_qk
+    _need(q, "q", torch.bfloat16, (T, H, D))
+    _need(kv, "kv", torch.bfloat16, (S_kv, D))
     _need(topk_idxs, "topk_idxs", torch.int32, (T, W))
     if topk_length is not None:
         _need(topk_length, "topk_length", torch.int32, (T,))
@@ -210,8 +212,8 @@ def fwd(q, kv, topk_idxs, topk_length=None, sink=None, scale=None, out=None, lse
     return out, lse
 
 
-def bwd_workspace_bytes(T, H, S_kv, W, scale=1.0 / 24.0, deterministic=False) -> int:
-    prob = make_problem(T, H, S_kv, W, scale, FLAG_DETERMINISTIC if deterministic else 0)
+def bwd_workspace_bytes(T, H, S_kv, W, scale=1.0 / 24.0, deterministic=False, d_qk=576) -> int:
+    prob = make_problem(T, H, S_kv, W, scale, FLAG_DETERMINISTIC if deterministic else 0, d_qk)
     return int(library().dsa_bwd_workspace_bytes(ctypes.byref(prob)))
 
 
@@ -229,8 +231,9 @@ def bwd(q, kv, topk_idxs, topk_length, sink, out, lse, dout, scale=None, dq=None
     flags = (FLAG_DELTA_RESIDUAL if delta_residual else 0) | \
         (FLAG_DETERMINISTIC if deterministic else 0)
     prob, (T, H, S_kv, W) = _problem_from(q, kv, topk_idxs, scale, flags)
-    _need(q, "q", torch.bfloat16, (T, H, 576))
-    _need(kv, "kv", torch.bfloat16, (S_kv, 576))
+    D = prob.d_qk
+    _need(q, "q", torch.bfloat16, (T, H, D))
+    _need(kv, "kv", torch.bfloat16, (S_kv, D))
     _need(topk_idxs, "topk_idxs", torch.int32, (T, W))
     if topk_length is not None:
         _need(topk_length, "topk_length", torch.int32, (T,))
@@ -243,9 +246,9 @@ def bwd(q, kv, topk_idxs, topk_length, sink, out, lse, dout, scale=None, dq=None
         _need_residual_room(out, T, H)
     dev = q.device
     if dq is None:
-        dq = torch.empty(T, H, 576, dtype=torch.bfloat16, device=dev)
+        dq = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
     if dkv is None:
-        dkv = torch.empty(S_kv, 576, dtype=torch.bfloat16, device=dev)
+        dkv = torch.empty(S_kv, D, dtype=torch.bfloat16, device=dev)
     if sink is not None and dsink is None:
         dsink = torch.empty(H, dtype=torch.float32, device=dev)
     nbytes = int(library().dsa_bwd_workspace_bytes(ctypes.byref(prob)))

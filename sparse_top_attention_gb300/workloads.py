@@ -139,12 +139,14 @@ def _compact(idx: np.ndarray, S_kv: int):
 
 
 def dsv4(T: int, H: int, topk: int, compact: bool, seed: int, name: str,
-         value_device: str = "cpu") -> Workload:
+         value_device: str = "cpu", d_qk: int = D_QK) -> Workload:
     """DeepSeek-V4-like layout: KV = T original rows + T/4 compressed rows.
 
     ``value_device`` chooses where q, kv, dout and sink are drawn (a seeded
     generator on that device); indices are always drawn on the host.  The two
-    choices give different values from the same distributions.
+    choices give different values from the same distributions.  ``d_qk`` is
+    the row width: 576 (512 V + 64 rope) or 512 (V only, the width of the
+    flash-attention page's performance table).
     """
     rng = np.random.default_rng(seed)
     gen = torch.Generator(device=value_device).manual_seed(seed)
@@ -153,28 +155,30 @@ def dsv4(T: int, H: int, topk: int, compact: bool, seed: int, name: str,
     length = None
     if compact:
         idx, length = _compact(idx, S_kv)
-    q = _randn_bf16(gen, (T, H, D_QK))
-    kv = _randn_bf16(gen, (S_kv, D_QK))
+    q = _randn_bf16(gen, (T, H, d_qk))
+    kv = _randn_bf16(gen, (S_kv, d_qk))
     dout = _randn_bf16(gen, (T, H, D_V))
     sink = torch.randn(H, generator=gen, dtype=torch.float32, device=gen.device)
     dev = gen.device
     return Workload(name, q, kv, torch.from_numpy(idx.astype(np.int32)).to(dev),
                     None if length is None else torch.from_numpy(length.astype(np.int32)).to(dev),
-                    sink, dout, 1.0 / math.sqrt(D_QK),
+                    sink, dout, 1.0 / math.sqrt(d_qk),
                     {"T": T, "H": H, "S_kv": S_kv, "W": 128 + topk, "topk": topk,
                      "compact": compact, "seed": seed})
 
 
-def varlen(lengths, H: int, topk: int, compact: bool, seed: int) -> Workload:
+def varlen(lengths, H: int, topk: int, compact: bool, seed: int,
+           value_device: str = "cpu", d_qk: int = D_QK) -> Workload:
     """A varlen batch of DeepSeek-V4-like sequences, packed.
 
     Sequence b has T_b = lengths[b] tokens and T_b + T_b // 4 KV rows, laid out
     as in ``dsv4`` with indices counted from its own first KV row.  All rows
     are padded to the same width 128 + topk.  A length of 0 gives an empty
-    sequence (no tokens, no KV rows).
+    sequence (no tokens, no KV rows).  ``value_device`` chooses where q, kv,
+    dout and sink are drawn, as in ``dsv4``.
     """
     rng = np.random.default_rng(seed)
-    gen = torch.Generator().manual_seed(seed)
+    gen = torch.Generator(device=value_device).manual_seed(seed)
     W = 128 + topk
     idx_parts, len_parts, cu_q, cu_kv = [], [], [0], [0]
     for T_b in lengths:
@@ -189,16 +193,20 @@ def varlen(lengths, H: int, topk: int, compact: bool, seed: int) -> Workload:
         cu_kv.append(cu_kv[-1] + S_b)
     T, S_kv = cu_q[-1], cu_kv[-1]
     idx = np.concatenate(idx_parts, axis=0) if idx_parts else np.zeros((0, W), np.int64)
-    q = _randn_bf16(gen, (T, H, D_QK))
-    kv = _randn_bf16(gen, (S_kv, D_QK))
+    q = _randn_bf16(gen, (T, H, d_qk))
+    kv = _randn_bf16(gen, (S_kv, d_qk))
     dout = _randn_bf16(gen, (T, H, D_V))
-    sink = torch.randn(H, generator=gen, dtype=torch.float32)
-    length = torch.from_numpy(np.concatenate(len_parts).astype(np.int32)) if compact else None
-    return Workload(f"varlen{list(lengths)}", q, kv, torch.from_numpy(idx.astype(np.int32)),
-                    length, sink, dout, 1.0 / math.sqrt(D_QK),
+    sink = torch.randn(H, generator=gen, dtype=torch.float32, device=gen.device)
+    dev = gen.device
+    length = (torch.from_numpy(np.concatenate(len_parts).astype(np.int32)).to(dev)
+              if compact else None)
+    return Workload(f"varlen{list(lengths)}", q, kv,
+                    torch.from_numpy(idx.astype(np.int32)).to(dev), length, sink, dout,
+                    1.0 / math.sqrt(d_qk),
                     {"lengths": list(lengths), "H": H, "topk": topk, "compact": compact,
                      "seed": seed},
-                    torch.tensor(cu_q, dtype=torch.int32), torch.tensor(cu_kv, dtype=torch.int32))
+                    torch.tensor(cu_q, dtype=torch.int32, device=dev),
+                    torch.tensor(cu_kv, dtype=torch.int32, device=dev))
 
 
 def tiny(seed: int = 1000) -> Workload:

@@ -56,7 +56,7 @@ def test_workspace_size_is_pure_host(lib):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(H=0), 1), (dict(H=129), 2), (dict(T=-1), 1), (dict(W=0), 1), (dict(S_kv=0), 1),
-    (dict(d_qk=512), 2), (dict(d_v=576), 2), (dict(flags=4), 1), (dict(scale=float("nan")), 1),
+    (dict(d_qk=256), 2), (dict(d_v=576), 2), (dict(flags=4), 1), (dict(scale=float("nan")), 1),
     (dict(W=4096), 2), (dict(S_kv=3728271), 2),
 ])
 def test_forward_rejects_before_launch(lib, kw, code):

@@ -129,15 +129,18 @@ def test_forward_matches_dense_sink_column(seed):
     np.testing.assert_allclose(r["lse"][rows], lse.numpy()[rows], rtol=1e-13)
 
 
-def test_backward_matches_torch_autograd():
+# (8, 6): rows wider than V, as with the 64 rope columns; (6, 6): rows that are
+# all V, as in the D = 512 variant.
+@pytest.mark.parametrize("D,d_v", [(8, 6), (6, 6)])
+def test_backward_matches_torch_autograd(D, d_v):
     """All gradients against fp64 autograd of the dense sink-column form."""
-    p = small_problem(5, T=6, H=3, S_kv=9, W=7, D=8, d_v=6)
+    p = small_problem(5, T=6, H=3, S_kv=9, W=7, D=D, d_v=d_v)
     g = run_bwd(p)
     mask = torch.from_numpy(dense_mask(p))
     q = torch.from_numpy(p["q"]).requires_grad_()
     kv = torch.from_numpy(p["kv"]).requires_grad_()
     sk = torch.from_numpy(p["sink"]).requires_grad_()
-    out, _ = dense_torch(q, kv, mask, sk, p["scale"], 6)
+    out, _ = dense_torch(q, kv, mask, sk, p["scale"], d_v)
     # every token here has >= 1 valid slot, so the dense form is defined everywhere
     assert mask.any(dim=1).all()
     (out * torch.from_numpy(p["dout"])).sum().backward()
@@ -146,9 +149,10 @@ def test_backward_matches_torch_autograd():
     np.testing.assert_allclose(g["dsink"], sk.grad.numpy(), rtol=1e-11, atol=1e-13)
 
 
-def test_backward_finite_differences():
+@pytest.mark.parametrize("D,d_v", [(8, 6), (6, 6)])
+def test_backward_finite_differences(D, d_v):
     """Central differences of l = sum(dout * out) for q, kv and sink in fp64."""
-    p = small_problem(6, T=5, H=3, S_kv=7, W=6, D=8, d_v=6)
+    p = small_problem(6, T=5, H=3, S_kv=7, W=6, D=D, d_v=d_v)
     g = run_bwd(p)
 
     def loss(pp):
@@ -442,7 +446,7 @@ def _pin_suite(monkeypatch_ctx=None):
     """Run the core pins and report how many fail."""
     fails = 0
     for fn in (lambda: test_forward_matches_dense_sink_column(3),
-               test_backward_matches_torch_autograd,
+               lambda: test_backward_matches_torch_autograd(8, 6),
                test_empty_rows,
                test_valid_indices_beyond_column_s_kv_count,
                lambda: test_positive_saturating_sink(1e38)):
