@@ -226,7 +226,8 @@ __device__ __forceinline__ uint32_t hs_tile_off(uint32_t h, uint32_t slot) {
 template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
 k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-         const __grid_constant__ CUtensorMap tm_sp, const __nv_bfloat16* __restrict__ kv,
+         const __grid_constant__ CUtensorMap tm_sp, const __grid_constant__ CUtensorMap tm_kv,
+         const __nv_bfloat16* __restrict__ kv,
          const int32_t* __restrict__ idxc, const int32_t* __restrict__ count,
          const float* __restrict__ lse2_g, const float* __restrict__ gate_g,
          const float* __restrict__ delta_g, __nv_bfloat16* __restrict__ dq, int T, int H, int W,
@@ -334,10 +335,30 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         dst[k] = sw128_off(row & (kBlk - 1), pc);
         nbytes[k] = ok ? 16u : 0u;
       }
+      // A full block of consecutive KV rows (the sliding window) comes in with
+      // one 2-D TMA load per chunk instead of 128 row copies.
+      bool contig = false;
+      int r0 = 0;
+      if (b * kBlk + kBlk <= Kt) {
+        r0 = rows[b * kBlk];
+        bool mine = true;
+        for (int i = tid - 160; i < kBlk; i += kProducers) mine &= rows[b * kBlk + i] == r0 + i;
+        contig = !named_bar_or(2, kProducers, !mine);
+      }
       for (int i = 0; i < kCh; ++i) {
         const int pos = pos_of_step<kRope>(i);
         if (b > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (b - 1) & 1, fs, 1);
         const int x = dchunk_of_pos<kRope>(pos);
+        if (contig) {
+          if (tid == 160) {
+            mbar_arrive_expect_tx(smem_u32(&m.kv_full[pos]), kKVChunk);
+            tma_load_2d_hint(sbase + kOffKV + pos * kKVChunk, &tm_kv, x * 64, r0,
+                             smem_u32(&m.kv_full[pos]), keep);
+          } else {
+            mbar_arrive(smem_u32(&m.kv_full[pos]));
+          }
+          continue;
+        }
 #pragma unroll
         for (int k = 0; k < kRowGroups; ++k)
           if (pw + 3 * k < kBlk / 4)
@@ -808,16 +829,18 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     const int G = bwd_groups(p.H), nbmax = bwd_nbmax(p.W);
     __nv_bfloat16* sp = reinterpret_cast<__nv_bfloat16*>(base + L.sp);
     const long long sp_rows = static_cast<long long>(p.T) * nbmax * 64 * G;
-    CUtensorMap tm_q, tm_do, tm_sp_st;
+    CUtensorMap tm_q, tm_do, tm_sp_st, tm_kv;
     const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
     e = make_head_tile_map(&tm_q, q, p.T, p.H, p.d_qk, box_heads);
     if (e == cudaSuccess) e = make_head_tile_map(&tm_do, dout, p.T, p.H, kDv, box_heads);
     if (e == cudaSuccess) e = make_matrix_map(&tm_sp_st, sp, sp_rows, kBlk, 32);
+    if (e == cudaSuccess) e = make_matrix_map(&tm_kv, kv, p.S_kv, p.d_qk, kBlk);
     if (e != cudaSuccess) return e;
     auto kern = p.d_qk == 512 ? k_bwd_dq<512> : k_bwd_dq<576>;
     const int smem = p.d_qk == 512 ? DqLayout<512>::kSmemBytes : DqLayout<576>::kSmemBytes;
     kern<<<static_cast<unsigned>(static_cast<long long>(p.T) * G), kThreads, smem, s>>>(
-        tm_q, tm_do, tm_sp_st, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2, gate,
+        tm_q, tm_do, tm_sp_st, tm_kv, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2,
+        gate,
         delta, static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, box_heads, nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -99,7 +99,8 @@ __device__ __forceinline__ void mbar_wait_final(uint32_t bar, uint32_t parity) {
 
 template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
-fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
+fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+           const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
            const float* __restrict__ sink, __nv_bfloat16* __restrict__ out,
            float* __restrict__ lse, const __nv_bfloat16* __restrict__ kv, int T, int H, int S_kv,
            int W, float scale, int G, int residual, int box_heads,
@@ -208,8 +209,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const int32_t* __restrict__
         dst[k] = sw128_off(row & (kBlk - 1), pc);
         nbytes[k] = ok ? 16u : 0u;
       }
+      // A full block of consecutive KV rows (the sliding window) comes in with
+      // one 2-D TMA load per chunk instead of 128 row copies.
+      bool contig = false;
+      int r0 = 0;
+      if (b * kBlk + kBlk <= Kt) {
+        r0 = list[b * kBlk];
+        bool mine = true;
+        for (int i = tid - kQIssuer; i < kBlk; i += kProducers) mine &= list[b * kBlk + i] == r0 + i;
+        contig = !named_bar_or(2, kProducers, !mine);
+      }
       for (int c = 0; c < kCh; ++c) {
         if (b > 0) mbar_wait(smem_u32(&m.kv_free[c]), (b - 1) & 1, fs, 1);
+        if (contig) {
+          if (tid == kQIssuer) {
+            mbar_arrive_expect_tx(smem_u32(&m.kv_full[c]), kKVChunk);
+            tma_load_2d_hint(sbase + kOffKV + c * kKVChunk, &tm_kv, c * 64, r0,
+                             smem_u32(&m.kv_full[c]), keep);
+          } else {
+            mbar_arrive(smem_u32(&m.kv_full[c]));
+          }
+          continue;
+        }
 #pragma unroll
         for (int k = 0; k < kRowGroups; ++k)
           if (pw + 3 * k < kBlk / 4)
@@ -421,14 +442,15 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const in
   const int G = (p.H + kHG - 1) / kHG;
   const long long grid = static_cast<long long>(p.T) * G;
   if (grid == 0) return cudaSuccess;
-  CUtensorMap tm_q;
+  CUtensorMap tm_q, tm_kv;
   const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
   cudaError_t e = make_head_tile_map(&tm_q, q, p.T, p.H, p.d_qk, box_heads);
+  if (e == cudaSuccess) e = make_matrix_map(&tm_kv, kv, p.S_kv, p.d_qk, kBlk);
   if (e != cudaSuccess) return e;
   auto kern = p.d_qk == 512 ? fwd_kernel<512> : fwd_kernel<576>;
   const int smem = p.d_qk == 512 ? FwdLayout<512>::kSmemBytes : FwdLayout<576>::kSmemBytes;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(
-      tm_q, idx, len, sink, static_cast<__nv_bfloat16*>(out), lse,
+      tm_q, tm_kv, idx, len, sink, static_cast<__nv_bfloat16*>(out), lse,
       static_cast<const __nv_bfloat16*>(kv), p.T, p.H, p.S_kv, p.W, p.scale, G,
       p.delta_residual ? 1 : 0, box_heads, p.cu_q, p.cu_kv, p.B);
   return cudaGetLastError();
