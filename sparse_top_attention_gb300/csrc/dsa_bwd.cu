@@ -529,7 +529,11 @@ constexpr int kBTile = 64 * 4 * 128 * 2;    // up to 256 rows x 128 slots bf16 =
 constexpr int kAStage = 4 * 128 * 128;      // Q and dO, 2 boxes each of up to 128 heads x 64 d
 constexpr int kOffB = 0;
 constexpr int kOffA = kOffB + kBTile;       // 2 stages
-constexpr int kOffMisc = kOffA + 2 * kAStage;
+// Drain staging: per slot quarter, 16 slots x 128 d fp32, so that one warp
+// reduction covers 128 contiguous floats of one KV row.
+constexpr int kStageQ = 16 * 128 * 4;
+constexpr int kOffStage = kOffA + 2 * kAStage;
+constexpr int kOffMisc = kOffStage + 4 * kStageQ;
 constexpr uint32_t kTmemCols = 256;         // 2 accumulators of 128 columns
 
 struct Misc {
@@ -693,21 +697,39 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         tc_fence_before();
         mbar_arrive(smem_u32(&m.d_empty[st]));
         const int d = n * 128 + sp * 32 + lane;
-        if (n < 4 || d < kD) {
-          if constexpr (kDet) {
+        if (kDet && (n < 4 || d < kD)) {
+          {
             unsigned long long* dst = static_cast<unsigned long long*>(dkv_acc) + d;
 #pragma unroll
             for (int s = 0; s < 32; ++s) {
               const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
               if (s < nvalid) red_add_fixed32(dst + o, __uint_as_float(v[s]), keep);
             }
-          } else {
-            float* dst = static_cast<float*>(dkv_acc) + d;
+          }
+        }
+        if constexpr (!kDet) {
+          // The quarter's four warps hold d rows 32 sp .. of the tile for the
+          // same 32 slots.  Through shared memory, 16 slots at a time, each
+          // warp then adds whole 128-float rows: 4 slots per warp, 32 lanes x
+          // 4 floats each (the fast reduction pattern).
+          float* stg = reinterpret_cast<float*>(smem + dkv::kOffStage) + quarter * (16 * 128);
+          const int dt = n * 128;  // first d of the tile
+          const bool lane_ok = dt + lane * 4 < kD;  // the rope tile has 64 columns
 #pragma unroll
-            for (int s = 0; s < 32; ++s) {
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int s = 0; s < 16; ++s) stg[s * 128 + sp * 32 + lane] = __uint_as_float(v[half * 16 + s]);
+            named_bar_sync(1 + quarter, 128);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int sl = sp * 4 + j;            // slot within the half
+              const int s = half * 16 + sl;         // slot within the quarter
+              const float4 f = *reinterpret_cast<const float4*>(stg + sl * 128 + lane * 4);
               const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
-              if (s < nvalid) red_add_f32_hint(dst + o, __uint_as_float(v[s]), keep);
+              if (s < nvalid && lane_ok)
+                red_add_v4_f32_hint(static_cast<float*>(dkv_acc) + o + dt + lane * 4, f, keep);
             }
+            named_bar_sync(1 + quarter, 128);
           }
         }
       }

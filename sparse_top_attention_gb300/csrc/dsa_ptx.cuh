@@ -221,6 +221,13 @@ __device__ __forceinline__ float fixed32_to_float(long long a) {
   return __ll2float_rn(a) * 2.3283064365386963e-10f;  // 2^-32
 }
 
+// Four consecutive fp32 adds (16-byte aligned) in one reduction.
+__device__ __forceinline__ void red_add_v4_f32_hint(float* addr, float4 v, uint64_t pol) {
+  asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+
 // fp32 add into global memory without a return value, with an L2 policy.
 __device__ __forceinline__ void red_add_f32_hint(float* addr, float v, uint64_t pol) {
   asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(pol)
