@@ -303,27 +303,36 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         s[i] = valid ? __uint_as_float(r0[i]) * sl2 : -INFINITY;
         s[32 + i] = valid ? __uint_as_float(r1[i]) * sl2 : -INFINITY;
       }
-      // column (per-head) maximum over the 128 gathered rows
-      float* red = m.red[b & 1][warp];
+      // Lazy rescale: a head keeps its shift unless the block's maximum
+      // exceeds it by more than 2^8; the final normalisation uses the same
+      // shift for O and l.  The column maxima are only needed when some score
+      // is that far above its head's shift (always in the first block), so
+      // one vote decides whether to compute them.
+      bool above = false;
 #pragma unroll
-      for (int h = 0; h < kHG; ++h) {
-        const float mx = warp_max(s[h]);
-        if ((h & 31) == lane) red[h] = mx;
+      for (int h = 0; h < kHG; ++h) above |= s[h] > m.m_used[h] + 8.f;
+      bool any = named_bar_or(1, 128, above);
+      if (any) {
+        // column (per-head) maximum over the 128 gathered rows
+        float* red = m.red[b & 1][warp];
+#pragma unroll
+        for (int h = 0; h < kHG; ++h) {
+          const float mx = warp_max(s[h]);
+          if ((h & 31) == lane) red[h] = mx;
+        }
+        named_bar_sync(1, 128);
+        bool resc = false;
+        if (tid < kHG) {
+          const float bm = fmaxf(fmaxf(m.red[b & 1][0][tid], m.red[b & 1][1][tid]),
+                                 fmaxf(m.red[b & 1][2][tid], m.red[b & 1][3][tid]));
+          const float mo = m.m_used[tid];
+          const float mn = fmaxf(mo, bm);
+          resc = mn > mo + 8.f;
+          m.fac[tid] = resc ? ex2_approx(mo - mn) : 1.f;
+          if (resc) m.m_used[tid] = mn;
+        }
+        any = named_bar_or(1, 128, resc);
       }
-      named_bar_sync(1, 128);
-      bool resc = false;
-      if (tid < kHG) {
-        const float bm = fmaxf(fmaxf(m.red[b & 1][0][tid], m.red[b & 1][1][tid]),
-                               fmaxf(m.red[b & 1][2][tid], m.red[b & 1][3][tid]));
-        const float mo = m.m_used[tid];
-        const float mn = fmaxf(mo, bm);
-        // Lazy rescale: keep the old shift unless the max grew by more than
-        // 2^8; the final normalisation uses the same shift for O and l.
-        resc = mn > mo + 8.f;
-        m.fac[tid] = resc ? ex2_approx(mo - mn) : 1.f;
-        if (resc) m.m_used[tid] = mn;
-      }
-      const bool any = named_bar_or(1, 128, resc);
       if (any) {
 #pragma unroll
         for (int h = 0; h < kHG; ++h) lp[h] *= m.fac[h];
