@@ -329,6 +329,7 @@ def run_ours(args, rank, world, local):
 
     varlen_leg = run_varlen_leg(args, dev, stream)
     d512_leg = run_d512_leg(args, dev, stream)
+    small_h_leg = run_small_h_leg(args, dev, stream)
 
     # End to end through the public API: pinned host inputs -> device, fwd + bwd,
     # outputs -> pinned host, every step.
@@ -361,6 +362,7 @@ def run_ours(args, rank, world, local):
             "bwd_deterministic_ms": bwd_det_ms,
             "varlen": varlen_leg,
             "d512": d512_leg,
+            "small_h": small_h_leg,
             "fwd_tflops": fwd_tflops,
             "bwd_finalize_tflops": bwd_dkv_flops / (fin_ms * 1e-3) / 1e12,
             "roofline": {"kernel": "k_bwd_dq", "bound": "tensor", "achieved": main_tflops,
@@ -459,6 +461,45 @@ def run_d512_leg(args, dev, stream):
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
             "bwd_tflops": 2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12}
+
+
+def run_small_h_leg(args, dev, stream):
+    """The headline layout at fewer heads (H = 16, 64): fwd + bwd per step.
+    The kernels put heads on the MMA N side, so a gathered block costs about
+    the same at any H up to the head group; the time per token, not per
+    head, is what stays put."""
+    from sparse_top_attention_gb300 import dsa
+    from sparse_top_attention_gb300 import workloads as WL
+    res = {}
+    for H in (16, 64):
+        w = WL.dsv4(T=WORKLOAD["T"], H=H, topk=WORKLOAD["topk"], compact=False, seed=1008,
+                    name=f"flash_t8k_h{H}", value_device=str(dev))
+        sum_k = float(WL.valid_slot_count_formula(w.T, WORKLOAD["topk"]).sum())
+        flops = 3.5 * FWD_FLOPS_PER_SLOT_HEAD * H * sum_k
+        out = torch.empty(w.T, H, 512, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(w.T, H, dtype=torch.float32, device=dev)
+        ws = torch.empty(dsa.bwd_workspace_bytes(w.T, H, w.S_kv, w.W), dtype=torch.uint8,
+                         device=dev)
+
+        def step():
+            dsa.fwd(w.q, w.kv, w.topk_idxs, None, w.sink, w.scale, out=out, lse=lse)
+            dsa.bwd(w.q, w.kv, w.topk_idxs, None, w.sink, out, lse, w.dout, w.scale, workspace=ws)
+
+        for _ in range(args.warmup):
+            step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert dsa.device_status() == 0
+        ms = e0.elapsed_time(e1) / args.steps
+        res[f"H{H}"] = {"ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                        "us_per_token": ms * 1e3 / w.T}
+        del w, out, lse, ws
+    return res
 
 
 def run_e2e(args, w, dev, stream, step_flops, world):
