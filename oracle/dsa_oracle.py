@@ -25,7 +25,7 @@ fusion.  Sources, cited by page title and section:
 [P1] NeMo Automodel PR 3467 (TileLang sparse-MLA backward fix): ValidMask is
      (idx >= 0) & (idx < S_kv).
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent:
 
 * The LSE excludes the sink.  The backward folds the sink in through
   sigma(LSE - sink) [P2 Summary 3, Why 3].

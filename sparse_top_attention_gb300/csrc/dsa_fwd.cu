@@ -13,8 +13,8 @@
 //   out = O * sigma(lse - sink) / l.
 // Sources:
 //   - flash-attention "[CuTe, SM100] Support 1..128 Q heads in sparse MLA via
-//     in-kernel TMA padding", Agent Notes: one token and one top-k gather list
-//     per tile; padded heads are zero rows.
+//     in-kernel TMA padding", Agent Notes: a tile serves a single token with
+//     its own top-k gather list; padded heads are zero rows.
 //   - cuDNN frontend "DSA backward SM90: fix three top-k and attention-sink
 //     boundary failures", Summary 1-3: empty rows, padded columns masked to
 //     -inf, a sink that stays finite when it saturates.

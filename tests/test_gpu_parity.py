@@ -65,9 +65,9 @@ def oracle_all(w, dout=None, tokens=None):
     bf16-stored forward output.  That is the backward's contract (delta =
     rowsum(dout * out) of the out handed in), and it is how the cuDNN page
     "DSA backward SM90: fix three top-k and attention-sink boundary failures"
-    ("Not addressed") checks its kernel: against the fp64 result recomputed
-    from the BF16-stored out.  The bf16 out is derived from the oracle, never
-    from the GPU."""
+    ("Not addressed") checks its kernel: an fp64 recomputation that starts
+    from the bf16 output the forward stored.  The bf16 out is derived from
+    the oracle, never from the GPU."""
     ref = O.forward(w.q, w.kv, w.topk_idxs, w.topk_length, w.sink, w.scale, tokens=tokens)
     g = O.backward(w.q, w.kv, w.topk_idxs, w.topk_length, w.sink, w.scale,
                    w.dout if dout is None else dout, out=bf16_stored(ref["out"]), tokens=tokens)

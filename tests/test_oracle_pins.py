@@ -256,7 +256,7 @@ def test_empty_rows():
 
 @pytest.mark.parametrize("big", [1e38, 2.4e38, O.FLT_MAX, math.inf])
 def test_positive_saturating_sink(big):
-    """sink -> +big: the sink takes the whole denominator, so out = dq = dkv = 0
+    """sink -> +big: exp(sink) dominates the denominator, so out = dq = dkv = 0
     and d_sink = -sum_t delta for a supplied nonzero O [P2 Testing]."""
     p = small_problem(12, T=5, H=3, S_kv=9, W=6, D=8, d_v=6, sink=big)
     r, g = run_fwd(p), run_bwd(p)
