@@ -261,12 +261,40 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   const int nblk = (Kt + kBlk - 1) / kBlk;
   const int32_t* rows = idxc + static_cast<size_t>(t) * W;
 
+  // Work whose latency the set-up below hides: the Q / dO tile loads (their
+  // issuing thread owns their barrier), the per-head rows of the preprocess,
+  // and each gather lane's row indices of the first block.
+  if (tid == 160) {
+    mbar_init(smem_u32(&m.qd_full), 1);
+    mbar_init_fence();
+    const uint64_t pol = l2_evict_first();
+    mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kCh + 8) * box_heads * 128);
+    for (int c = 0; c < kCh; ++c)
+      tma_load_3d_hint(sbase + kOffQD + c * kQdO, &tm_q, c * 64, h0, t, smem_u32(&m.qd_full),
+                       pol);
+    for (int c = 0; c < 8; ++c)
+      tma_load_3d_hint(sbase + kOffQD + c * kQdO + kHChunk, &tm_do, c * 64, h0, t,
+                       smem_u32(&m.qd_full), pol);
+  }
+  float pre_lse2 = 0.f, pre_gate = 0.f, pre_delta = 0.f;
+  if (tid < nh) {  // padded heads keep gate 0, hence P = dS = 0: they add nothing
+    const size_t r = static_cast<size_t>(t) * H + h0 + tid;
+    pre_lse2 = lse2_g[r];
+    pre_gate = gate_g[r];
+    pre_delta = delta_g[r];
+  }
+  int pre_rows[kRowGroups];
+#pragma unroll
+  for (int k = 0; k < kRowGroups; ++k) {
+    const int g = (warp - 5) + 3 * k, slot = g * 4 + (lane >> 3);
+    pre_rows[k] = (warp >= 5 && g < kBlk / 4 && slot < Kt) ? rows[slot] : 0;
+  }
+
   if (tid == 0) {
     for (int c = 0; c < kCh; ++c) {
       mbar_init(smem_u32(&m.kv_full[c]), kProducers);
       mbar_init(smem_u32(&m.kv_free[c]), 1);
     }
-    mbar_init(smem_u32(&m.qd_full), 1);
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.ds_full), 128);
     mbar_init(smem_u32(&m.rope_done), 1);
@@ -277,12 +305,9 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     mbar_init_fence();
   }
   if (tid < kHG) {
-    const bool real = tid < nh;
-    const size_t r = static_cast<size_t>(t) * H + h0 + tid;
-    // Padded heads get gate 0, hence P = dS = 0: they add nothing anywhere.
-    m.lse2[tid] = real ? lse2_g[r] : 0.f;
-    m.gate[tid] = real ? gate_g[r] : 0.f;
-    m.delta[tid] = real ? delta_g[r] : 0.f;
+    m.lse2[tid] = pre_lse2;
+    m.gate[tid] = pre_gate;
+    m.delta[tid] = pre_delta;
   }
   // Q / dO tile rows the TMA box does not cover (only when H < 32) are zero.
   for (int i = tid; i < (kCh + 8) * (kHG - box_heads) * 8; i += kThreads) {
@@ -308,16 +333,6 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     // cp.async (one warp instruction = 4 whole 128 B row pieces) into the
     // 128B-swizzled chunk tiles.
     const int pw = warp - 5;
-    if (tid == 160) {
-      const uint64_t pol = l2_evict_first();
-      mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kCh + 8) * box_heads * 128);
-      for (int c = 0; c < kCh; ++c)
-        tma_load_3d_hint(sbase + kOffQD + c * kQdO, &tm_q, c * 64, h0, t, smem_u32(&m.qd_full),
-                         pol);
-      for (int c = 0; c < 8; ++c)
-        tma_load_3d_hint(sbase + kOffQD + c * kQdO + kHChunk, &tm_do, c * 64, h0, t,
-                         smem_u32(&m.qd_full), pol);
-    }
     const uint64_t keep = l2_evict_last();
     for (int b = 0; b < nblk; ++b) {
       // This lane's rows of the block, read once (before the wait on the
@@ -330,7 +345,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         const int row = g * 4 + (lane >> 3), pc = lane & 7;
         const int slot = b * kBlk + row;
         const bool ok = g < kBlk / 4 && slot < Kt;
-        const int r = ok ? rows[slot] : 0;
+        const int r = b == 0 ? pre_rows[k] : (ok ? rows[slot] : 0);
         src[k] = kv + static_cast<size_t>(r) * kD + pc * 8;
         dst[k] = sw128_off(row & (kBlk - 1), pc);
         nbytes[k] = ok ? 16u : 0u;
