@@ -96,4 +96,47 @@ __device__ __forceinline__ int compact_token(const int32_t* __restrict__ idx_row
   return base;
 }
 
+// compact_token on a row that each thread has already read into registers:
+// vals[i] is entry i * nthreads + tid (W <= kN * nthreads).  Reading the row
+// early lets its latency overlap other set-up work.
+template <int kN>
+__device__ __forceinline__ void load_index_row(const int32_t* __restrict__ idx_row, int W, int tid,
+                                               int nthreads, int32_t (&vals)[kN]) {
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    const int j = i * nthreads + tid;
+    vals[i] = j < W ? idx_row[j] : -1;
+  }
+}
+
+template <int kN>
+__device__ __forceinline__ int compact_token_regs(const int32_t (&vals)[kN], int W, int len,
+                                                  KvRange kv, int32_t* list, int cap,
+                                                  int* warp_counts, int tid, int nthreads) {
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    if (i * nthreads >= W) break;
+    const int j = i * nthreads + tid;
+    const int32_t v = vals[i];
+    const bool ok = j < W && slot_valid(v, j, len, kv.n);
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    if (lane == 0) warp_counts[warp] = __popc(bal);
+    __syncthreads();
+    int off = base, tot = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int c = warp_counts[w];
+      if (w < warp) off += c;
+      tot += c;
+    }
+    const int pos = off + __popc(bal & lt_mask);
+    if (ok && pos < cap) list[pos] = kv.lo + v;
+    base += tot;
+    __syncthreads();
+  }
+  return base;
+}
+
 }  // namespace dsa

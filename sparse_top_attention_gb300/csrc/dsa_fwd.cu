@@ -122,12 +122,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   int32_t* list = reinterpret_cast<int32_t*>(smem + kOffList);
   const FailState fs{&g_err_fwd, &m.abort_flag};
 
+  // The Q tile of the head group (kCh chunks of [box_heads x 64 columns],
+  // 128B swizzle; heads past H inside the box are zero-filled by the TMA)
+  // loads from kernel entry: its issuing thread owns its barrier.  The
+  // token's index row is read into registers now as well, so that both
+  // latencies overlap the set-up below.
+  if (tid == kQIssuer) {
+    mbar_init(smem_u32(&m.q_full), 1);
+    mbar_init_fence();
+    mbar_arrive_expect_tx(smem_u32(&m.q_full), kCh * box_heads * 128);
+    const uint64_t pol = l2_evict_first();
+    for (int c = 0; c < kCh; ++c)
+      tma_load_3d_hint(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t, smem_u32(&m.q_full),
+                       pol);
+  }
+  int32_t idx_regs[kMaxW / kThreads];
+  load_index_row(topk_idxs + static_cast<size_t>(t) * W, W, tid, kThreads, idx_regs);
+
   if (tid == 0) {
     for (int c = 0; c < kCh; ++c) {
       mbar_init(smem_u32(&m.kv_full[c]), kProducers);
       mbar_init(smem_u32(&m.kv_free[c]), 1);
     }
-    mbar_init(smem_u32(&m.q_full), 1);
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.p_full), 128);
     mbar_init(smem_u32(&m.o_done), 1);
@@ -148,22 +164,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   }
   fence_proxy_async_smem();
   __syncthreads();
-  // The Q tile of the head group (9 chunks of [box_heads x 64 columns], 128B
-  // swizzle; heads past H inside the box are zero-filled by the TMA) loads
-  // while the slots are decoded.
-  if (tid == kQIssuer) {
-    mbar_arrive_expect_tx(smem_u32(&m.q_full), kCh * box_heads * 128);
-    const uint64_t pol = l2_evict_first();
-    for (int c = 0; c < kCh; ++c)
-      tma_load_3d_hint(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t, smem_u32(&m.q_full),
-                       pol);
-  }
 
   // a1: decode and compact the valid slots of token t (slot order).
   const int len = slot_len(topk_length, t, W);
   const KvRange kvr = kv_range(cu_q, cu_kv, B, t, S_kv);
-  const int Kt = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, kvr, list, kMaxW,
-                               m.warp_counts, tid, kThreads);
+  const int Kt = compact_token_regs(idx_regs, W, len, kvr, list, kMaxW, m.warp_counts, tid,
+                                    kThreads);
 
   const size_t lo_off = residual ? static_cast<size_t>(T) * H * kDv : 0;  // residual half
   if (Kt == 0) {  // empty row: out = 0, lse = -FLT_MAX, no tensor-core work
