@@ -209,6 +209,33 @@ def varlen(lengths, H: int, topk: int, compact: bool, seed: int,
                     torch.tensor(cu_kv, dtype=torch.int32, device=dev))
 
 
+def random_rows(T: int, H: int, S_kv: int, W: int, max_valid: int, seed: int,
+                compact: bool = False, d_qk: int = D_QK) -> Workload:
+    """Token t takes n_t ~ U{0..min(max_valid, W, S_kv)} distinct rows of [0, S_kv)
+    at random columns of W, the other columns -1 (or packed left with a
+    topk_length when ``compact``).  For limit cases: T = 1, W = 1, the
+    largest W, S_kv = 1, any H."""
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    idx = np.full((T, W), -1, dtype=np.int64)
+    cap = min(max_valid, W, S_kv)
+    for t in range(T):
+        n = int(rng.integers(0, cap + 1))
+        cols = rng.choice(W, size=n, replace=False)
+        idx[t, cols] = rng.choice(S_kv, size=n, replace=False)
+    length = None
+    if compact:
+        idx, length = _compact(idx, S_kv)
+    q = _randn_bf16(gen, (T, H, d_qk))
+    kv = _randn_bf16(gen, (S_kv, d_qk))
+    dout = _randn_bf16(gen, (T, H, D_V))
+    sink = torch.randn(H, generator=gen, dtype=torch.float32)
+    return Workload(f"random_T{T}_H{H}_S{S_kv}_W{W}", q, kv, torch.from_numpy(idx.astype(np.int32)),
+                    None if length is None else torch.from_numpy(length.astype(np.int32)),
+                    sink, dout, 1.0 / math.sqrt(d_qk),
+                    {"T": T, "H": H, "S_kv": S_kv, "W": W, "max_valid": max_valid, "seed": seed})
+
+
 def tiny(seed: int = 1000) -> Workload:
     """T=64, S_kv=64, H=16, width 32, non-compact causal rows."""
     T, S_kv, H, W = 64, 64, 16, 32
