@@ -503,48 +503,75 @@ def run_small_h_leg(args, dev, stream):
 
 
 def run_e2e(args, w, dev, stream, step_flops, world):
+    """Every step copies its inputs in from pinned host memory, runs fwd + bwd
+    and copies every output back out, as a training loop would.  The copies
+    of step i + 1 (in) and step i - 1 (out) overlap the compute of step i:
+    three streams, double-buffered device inputs and outputs, and events so
+    that no buffer is overwritten while a copy or kernel still uses it."""
     from sparse_top_attention_gb300 import dsa
     host = {k: getattr(w, k).cpu().pin_memory() for k in ("q", "kv", "topk_idxs", "sink", "dout")}
-    d = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
     T, H, S_kv, W = w.T, w.H, w.S_kv, w.W
-    outs = {"out": torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev),
-            "lse": torch.empty(T, H, dtype=torch.float32, device=dev),
-            "dq": torch.empty(T, H, 576, dtype=torch.bfloat16, device=dev),
-            "dkv": torch.empty(S_kv, 576, dtype=torch.bfloat16, device=dev),
-            "dsink": torch.empty(H, dtype=torch.float32, device=dev)}
-    hout = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+
+    def outputs():
+        return {"out": torch.empty(T, H, 512, dtype=torch.bfloat16, device=dev),
+                "lse": torch.empty(T, H, dtype=torch.float32, device=dev),
+                "dq": torch.empty(T, H, 576, dtype=torch.bfloat16, device=dev),
+                "dkv": torch.empty(S_kv, 576, dtype=torch.bfloat16, device=dev),
+                "dsink": torch.empty(H, dtype=torch.float32, device=dev)}
+
+    d = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
+    outs = [outputs() for _ in range(2)]
+    hout = [{k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs[0].items()}
+            for _ in range(2)]
     ws = torch.empty(dsa.bwd_workspace_bytes(T, H, S_kv, W), dtype=torch.uint8, device=dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout[0].values())
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    comp = stream
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, comp_done, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for e in comp_done + out_free:      # both buffer sets start free
+        e.record(comp)
 
-    def one():
-        for k in host:
-            d[k].copy_(host[k], non_blocking=True)
-        dsa.fwd(d["q"], d["kv"], d["topk_idxs"], None, d["sink"], w.scale, out=outs["out"],
-                lse=outs["lse"])
-        dsa.bwd(d["q"], d["kv"], d["topk_idxs"], None, d["sink"], outs["out"], outs["lse"],
-                d["dout"], w.scale, dq=outs["dq"], dkv=outs["dkv"], dsink=outs["dsink"],
-                workspace=ws)
-        for k in hout:
-            hout[k].copy_(outs[k], non_blocking=True)
+    def step(i):
+        u = i & 1
+        with torch.cuda.stream(s_in):   # inputs of step i (set u is free once step i-2 is done)
+            s_in.wait_event(comp_done[u])
+            for k in host:
+                d[u][k].copy_(host[k], non_blocking=True)
+            in_ready[u].record(s_in)
+        comp.wait_event(in_ready[u])
+        comp.wait_event(out_free[u])    # step i-2's outputs have been copied out
+        x, o = d[u], outs[u]
+        dsa.fwd(x["q"], x["kv"], x["topk_idxs"], None, x["sink"], w.scale, out=o["out"],
+                lse=o["lse"], stream=comp)
+        dsa.bwd(x["q"], x["kv"], x["topk_idxs"], None, x["sink"], o["out"], o["lse"], x["dout"],
+                w.scale, dq=o["dq"], dkv=o["dkv"], dsink=o["dsink"], workspace=ws, stream=comp)
+        comp_done[u].record(comp)
+        with torch.cuda.stream(s_out):  # outputs of step i
+            s_out.wait_event(comp_done[u])
+            for k in hout[u]:
+                hout[u][k].copy_(o[k], non_blocking=True)
+            out_free[u].record(s_out)
 
-    for _ in range(max(1, args.warmup)):
-        one()
+    for i in range(max(1, args.warmup)):
+        step(i)
     torch.cuda.synchronize()
     steps = max(1, min(args.steps, 10))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(steps):
-        one()
-    e1.record(stream)
+    e0.record(s_in)                     # before the first input copy
+    for i in range(steps):
+        step(i)
+    e1.record(s_out)                    # after the last output copy (it follows all other work)
     torch.cuda.synchronize()
+    assert dsa.device_status() == 0
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
     return {"value": world * step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms,
-            "steps": steps}
+            "steps": steps, "overlap": "copies of neighbouring steps overlap the compute"}
 
 
 def main():
