@@ -1,7 +1,7 @@
 // Sparse MLA (DSA) backward for sm_103a.
 //
 // Kernels, queued in order on the caller's stream:
-//   memset      fp32 dkv accumulator <- 0
+//   memset      dkv accumulator <- 0 (fp32, or int64 fixed point)
 //   k_compact   a1: valid KV rows of every token, in slot order, and counts
 //   k_bwd_pre   b1: delta = rowsum(dout * out), lse*log2(e), gate and the
 //               per-(t,h) d_sink terms (FlashAttention "dpsum" preprocess)
@@ -34,15 +34,20 @@
 //     width > total_S_kv": a dkv contribution is judged by the index value
 //     and the top-k bound only.
 //
+// Rows are D = 576 columns (512 V + 64 rope) or 512 (no rope part); the
+// kernels are templates over D.
 // k_bwd_dq tiles, transposed like the forward: gathered rows are UMMA M
 // (128) and the 32 heads of the group are N.
 //   [S^T | dP^T] = KV_blk . [Q^T | dO^T]  M=128 N=64  K=512, then S^T += rope part (N=32, K=64)
-//   dQ^T += KV_blk^T . dS'^T             5 x (M=128 N=32 K=128)
+//   dQ^T += KV_blk^T . dS'^T             ceil(D/128) x (M=128 N=32 K=128)
 // where dS' = scale * dS.  dS'^T and P^T tiles are written to the scratch.
+// A block of 128 consecutive KV rows (the sliding window) is loaded by 2-D
+// TMA; other blocks row by row with cp.async.
 // k_bwd_dkv tiles, per 128-slot block of one token, d rows on the M side:
 //   dKV_blk^T[d, slots] = [Q^T | dO^T][d, 2 x 32G] . [dS'; P][2 x 32G, slots]
 // (dO^T is zero for the 64 rope rows), so the dKV GEMM sees all heads at once
-// and each valid slot gets one partial per token.
+// and each valid slot gets one partial per token.  Its fp32 adds go through
+// shared memory so that each warp reduction covers 128 floats of one row.
 #include <cmath>
 
 #include "dsa_common.cuh"

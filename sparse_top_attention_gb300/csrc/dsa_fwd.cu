@@ -6,10 +6,12 @@
 // accumulators in TMEM, in a transposed orientation: the gathered rows form
 // the UMMA M dimension (128) and the heads form N (64), so a 64-head group
 // fills a full-rate M=128 tile.
-//   S^T[slot, h]  = sum_d KV[slot, d] * Q[h, d]          (M=128, N=64, K=576)
+//   S^T[slot, h]  = sum_d KV[slot, d] * Q[h, d]          (M=128, N=64, K=D)
 //   O^T[d, h]    += sum_slot V[slot, d] * P^T[slot, h]   (4 x M=128, N=64, K=128)
-// The softmax runs on S^T in registers, one thread per gathered row.  The
-// sink enters at the end, as sigma(lse - sink):
+// with rows of D = 576 columns (512 V + 64 rope) or 512 (a template
+// parameter).  The softmax runs on S^T in registers, one thread per gathered
+// row, with a lazy rescale: a head's shift only moves when a score exceeds it
+// by more than 2^8.  The sink enters at the end, as sigma(lse - sink):
 //   out = O * sigma(lse - sink) / l.
 // Sources:
 //   - flash-attention "[CuTe, SM100] Support 1..128 Q heads in sparse MLA via
@@ -22,9 +24,10 @@
 // Warp roles (256 threads):
 //   warps 0-3  softmax and epilogue; thread i owns TMEM lane i (gathered row i)
 //   warp 4     TMEM allocation and the single UMMA-issuing thread
-//   warps 5-7  lane 0 of warp 5 issues the Q tile TMA (3-D tensor map);
-//              then the three warps gather KV rows with cp.async into
-//              128B-swizzled shared tiles
+//   warps 5-7  lane 0 of warp 5 issues the Q tile TMA (3-D tensor map) at
+//              kernel entry; the three warps gather KV rows with cp.async into
+//              128B-swizzled shared tiles, or a whole block of consecutive
+//              rows (the sliding window) with 2-D TMA
 // Eight warps keep two warps per SM sub-partition, so each thread may use up
 // to 255 registers.
 #include <cmath>

@@ -228,12 +228,6 @@ __device__ __forceinline__ void red_add_v4_f32_hint(float* addr, float4 v, uint6
                : "memory");
 }
 
-// fp32 add into global memory without a return value, with an L2 policy.
-__device__ __forceinline__ void red_add_f32_hint(float* addr, float v, uint64_t pol) {
-  asm volatile("red.global.add.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(addr), "f"(v), "l"(pol)
-               : "memory");
-}
-
 // ----------------------------------------------------------------- tcgen05
 
 // Whole-warp TMEM allocation; the base address is written to `dst_smem`.
@@ -274,9 +268,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -304,26 +295,6 @@ __device__ __forceinline__ void tmem_ld32x2_sync(uint32_t ta, uint32_t (&r)[32],
       "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15]), "=r"(q[16]), "=r"(q[17]), "=r"(q[18]), "=r"(q[19]), "=r"(q[20]), "=r"(q[21]), "=r"(q[22]), "=r"(q[23]), "=r"(q[24]), "=r"(q[25]), "=r"(q[26]), "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
-      : "r"(ta), "r"(tb)
-      : "memory");
-}
-
-// Two 16-lane loads of an M = 64 accumulator (rows on lanes 0..15 of each
-// warp's quarter) and one wait.  Thread t < 16 gets lane t, columns
-// [c, c + 16); thread t >= 16 gets lane t - 16, columns [c + 16, c + 32).
-__device__ __forceinline__ void tmem_ld16x2_pair_sync(uint32_t ta, uint32_t (&r)[16], uint32_t tb,
-                                                      uint32_t (&q)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32], 16;\n\t"
-      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
-      "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33], 16;\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]),
-        "=r"(q[5]), "=r"(q[6]), "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]),
-        "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15])
       : "r"(ta), "r"(tb)
       : "memory");
 }
