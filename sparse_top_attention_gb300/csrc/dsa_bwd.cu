@@ -165,13 +165,16 @@ constexpr int kKVChunk = kBlk * 128;     // 16 KB
 constexpr int kHChunk = kHG * 128;       // 4 KB: 64 columns of 32 head rows
 constexpr int kQdO = 2 * kHChunk;                   // Q chunk x, then dO chunk x
 
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColdP = 32, kColdQ = 64;
+// TMEM: [S^T | dP^T] (64 columns), then two dQ^T buffers of 5 x 32 columns
+// so that one item's dQ is read out while the next item accumulates.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColdP = 32, kColdQ = 64, kDqCols = 160;
 
 struct Misc {
   uint64_t kv_full[kChunks];
   uint64_t kv_free[kChunks];
-  uint64_t qd_full, s_full, ds_full, rope_done, dsp_free, dq_done, mma_done;
+  uint64_t qd_full, qd_free, s_full, ds_full, rope_done, dsp_free, mma_done;
+  uint64_t dq_full[2], dq_free[2];  // the two dQ^T buffers, by item parity
   float lse2[kHG], gate[kHG], delta[kHG];
   uint32_t tmem_base;
   int abort_flag;
@@ -243,9 +246,6 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   constexpr bool kRope = L::kRope;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
-  const int h0 = grp * kHG;
-  const int nh = min(kHG, H - h0);
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {
     if (tid == 0) atomicCAS(&g_err_bwd, 0u, 0x2FFu);
@@ -253,74 +253,39 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   }
   Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const FailState fs{&g_err_bwd, &m.abort_flag};
-  const int Kt = count[t];
-
-  if (Kt == 0) {  // empty row: dq = 0, nothing for dkv
-    for (int v = tid; v < nh * (kD / 8); v += kThreads) {
-      const int h = v / (kD / 8), c = v - h * (kD / 8);
-      *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kD + c * 8) =
-          make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
-  const int nblk = (Kt + kBlk - 1) / kBlk;
-  const int32_t* rows = idxc + static_cast<size_t>(t) * W;
-
-  // Work whose latency the set-up below hides: the Q / dO tile loads (their
-  // issuing thread owns their barrier), the per-head rows of the preprocess,
-  // and each gather lane's row indices of the first block.
-  if (tid == 160) {
-    mbar_init(smem_u32(&m.qd_full), 1);
-    mbar_init_fence();
-    const uint64_t pol = l2_evict_first();
-    mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kCh + 8) * box_heads * 128);
-    for (int c = 0; c < kCh; ++c)
-      tma_load_3d_hint(sbase + kOffQD + c * kQdO, &tm_q, c * 64, h0, t, smem_u32(&m.qd_full),
-                       pol);
-    for (int c = 0; c < 8; ++c)
-      tma_load_3d_hint(sbase + kOffQD + c * kQdO + kHChunk, &tm_do, c * 64, h0, t,
-                       smem_u32(&m.qd_full), pol);
-  }
-  float pre_lse2 = 0.f, pre_gate = 0.f, pre_delta = 0.f;
-  if (tid < nh) {  // padded heads keep gate 0, hence P = dS = 0: they add nothing
-    const size_t r = static_cast<size_t>(t) * H + h0 + tid;
-    pre_lse2 = lse2_g[r];
-    pre_gate = gate_g[r];
-    pre_delta = delta_g[r];
-  }
-  int pre_rows[kRowGroups];
-#pragma unroll
-  for (int k = 0; k < kRowGroups; ++k) {
-    const int g = (warp - 5) + 3 * k, slot = g * 4 + (lane >> 3);
-    pre_rows[k] = (warp >= 5 && g < kBlk / 4 && slot < Kt) ? rows[slot] : 0;
-  }
+  // Persistent: CTA c takes items c, c + gridDim.x, ... of the (token, head
+  // group) list.  Every role walks the same items; barrier phases follow a
+  // running count of blocks (per-block barriers) and of non-empty items
+  // (per-item barriers).
+  const int n_items = T * G;
 
   if (tid == 0) {
     for (int c = 0; c < kCh; ++c) {
       mbar_init(smem_u32(&m.kv_full[c]), kProducers);
       mbar_init(smem_u32(&m.kv_free[c]), 1);
     }
+    mbar_init(smem_u32(&m.qd_full), 1);
+    mbar_init(smem_u32(&m.qd_free), 1);
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.ds_full), 128);
     mbar_init(smem_u32(&m.rope_done), 1);
     mbar_init(smem_u32(&m.dsp_free), 1);
-    mbar_init(smem_u32(&m.dq_done), 1);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(smem_u32(&m.dq_full[u]), 1);
+      mbar_init(smem_u32(&m.dq_free[u]), 128);
+    }
     mbar_init(smem_u32(&m.mma_done), 1);
     m.abort_flag = 0;
     mbar_init_fence();
   }
-  if (tid < kHG) {
-    m.lse2[tid] = pre_lse2;
-    m.gate[tid] = pre_gate;
-    m.delta[tid] = pre_delta;
-  }
-  // Q / dO tile rows the TMA box does not cover (only when H < 32) are zero.
+  // Q / dO tile rows the TMA box does not cover (only when H < 32) are zero;
+  // the loads never write them, so once is enough.
   for (int i = tid; i < (kCh + 8) * (kHG - box_heads) * 8; i += kThreads) {
     const int per = (kHG - box_heads) * 8;
     const int c = i / per, rem = i - c * per;
     const int row = box_heads + rem / 8, pc = rem & 7;
     const uint32_t base = c < kCh ? sbase + kOffQD + c * kQdO
-                                      : sbase + kOffQD + (c - kCh) * kQdO + kHChunk;
+                                  : sbase + kOffQD + (c - kCh) * kQdO + kHChunk;
     asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(base + sw128_off(row, pc)), "r"(0u)
                  : "memory");
   }
@@ -334,58 +299,80 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 
   if (warp >= 5) {
     // ------------------------------------------------------------ loads
-    // Q and dO tiles of the head group by TMA, then the KV row gather with
-    // cp.async (one warp instruction = 4 whole 128 B row pieces) into the
-    // 128B-swizzled chunk tiles.
+    // Per item: the Q and dO tiles of the head group by TMA (once the
+    // previous item's S / dP GEMMs are done with them), then the KV row
+    // gather with cp.async (one warp instruction = 4 whole 128 B row pieces)
+    // into the 128B-swizzled chunk tiles, or by 2-D TMA for a block of
+    // consecutive rows.
     const int pw = warp - 5;
     const uint64_t keep = l2_evict_last();
-    for (int b = 0; b < nblk; ++b) {
-      // This lane's rows of the block, read once (before the wait on the
-      // first chunk, so the reads overlap it) and reused by all 9 chunks.
-      const __nv_bfloat16* src[kRowGroups];
-      uint32_t dst[kRowGroups], nbytes[kRowGroups];
+    int gb = 0, it = 0;  // blocks and non-empty items so far
+    for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
+      const int t = u / G, h0 = (u - t * G) * kHG;
+      const int Kt = count[t];
+      if (Kt == 0) continue;
+      const int nblk = (Kt + kBlk - 1) / kBlk;
+      const int32_t* rows = idxc + static_cast<size_t>(t) * W;
+      if (tid == 160) {
+        if (it > 0) mbar_wait(smem_u32(&m.qd_free), (it - 1) & 1, fs, 11);
+        const uint64_t pol = l2_evict_first();
+        mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kCh + 8) * box_heads * 128);
+        for (int c = 0; c < kCh; ++c)
+          tma_load_3d_hint(sbase + kOffQD + c * kQdO, &tm_q, c * 64, h0, t,
+                           smem_u32(&m.qd_full), pol);
+        for (int c = 0; c < 8; ++c)
+          tma_load_3d_hint(sbase + kOffQD + c * kQdO + kHChunk, &tm_do, c * 64, h0, t,
+                           smem_u32(&m.qd_full), pol);
+      }
+      for (int b = 0; b < nblk; ++b, ++gb) {
+        // This lane's rows of the block, read once (before the wait on the
+        // first chunk, so the reads overlap it) and reused by all chunks.
+        const __nv_bfloat16* src[kRowGroups];
+        uint32_t dst[kRowGroups], nbytes[kRowGroups];
 #pragma unroll
-      for (int k = 0; k < kRowGroups; ++k) {
-        const int g = pw + 3 * k;
-        const int row = g * 4 + (lane >> 3), pc = lane & 7;
-        const int slot = b * kBlk + row;
-        const bool ok = g < kBlk / 4 && slot < Kt;
-        const int r = b == 0 ? pre_rows[k] : (ok ? rows[slot] : 0);
-        src[k] = kv + static_cast<size_t>(r) * kD + pc * 8;
-        dst[k] = sw128_off(row & (kBlk - 1), pc);
-        nbytes[k] = ok ? 16u : 0u;
-      }
-      // A full block of consecutive KV rows (the sliding window) comes in with
-      // one 2-D TMA load per chunk instead of 128 row copies.
-      bool contig = false;
-      int r0 = 0;
-      if (b * kBlk + kBlk <= Kt) {
-        r0 = rows[b * kBlk];
-        bool mine = true;
-        for (int i = tid - 160; i < kBlk; i += kProducers) mine &= rows[b * kBlk + i] == r0 + i;
-        contig = !named_bar_or(2, kProducers, !mine);
-      }
-      for (int i = 0; i < kCh; ++i) {
-        const int pos = pos_of_step<kRope>(i);
-        if (b > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (b - 1) & 1, fs, 1);
-        const int x = dchunk_of_pos<kRope>(pos);
-        if (contig) {
-          if (tid == 160) {
-            mbar_arrive_expect_tx(smem_u32(&m.kv_full[pos]), kKVChunk);
-            tma_load_2d_hint(sbase + kOffKV + pos * kKVChunk, &tm_kv, x * 64, r0,
-                             smem_u32(&m.kv_full[pos]), keep);
-          } else {
-            mbar_arrive(smem_u32(&m.kv_full[pos]));
-          }
-          continue;
+        for (int k = 0; k < kRowGroups; ++k) {
+          const int g = pw + 3 * k;
+          const int row = g * 4 + (lane >> 3), pc = lane & 7;
+          const int slot = b * kBlk + row;
+          const bool ok = g < kBlk / 4 && slot < Kt;
+          const int r = ok ? rows[slot] : 0;
+          src[k] = kv + static_cast<size_t>(r) * kD + pc * 8;
+          dst[k] = sw128_off(row & (kBlk - 1), pc);
+          nbytes[k] = ok ? 16u : 0u;
         }
+        // A full block of consecutive KV rows (the sliding window) comes in
+        // with one 2-D TMA load per chunk instead of 128 row copies.
+        bool contig = false;
+        int r0 = 0;
+        if (b * kBlk + kBlk <= Kt) {
+          r0 = rows[b * kBlk];
+          bool mine = true;
+          for (int i = tid - 160; i < kBlk; i += kProducers) mine &= rows[b * kBlk + i] == r0 + i;
+          contig = !named_bar_or(2, kProducers, !mine);
+        }
+        for (int i = 0; i < kCh; ++i) {
+          const int pos = pos_of_step<kRope>(i);
+          if (gb > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (gb - 1) & 1, fs, 1);
+          const int x = dchunk_of_pos<kRope>(pos);
+          if (contig) {
+            if (tid == 160) {
+              mbar_arrive_expect_tx(smem_u32(&m.kv_full[pos]), kKVChunk);
+              tma_load_2d_hint(sbase + kOffKV + pos * kKVChunk, &tm_kv, x * 64, r0,
+                               smem_u32(&m.kv_full[pos]), keep);
+            } else {
+              mbar_arrive(smem_u32(&m.kv_full[pos]));
+            }
+            continue;
+          }
 #pragma unroll
-        for (int k = 0; k < kRowGroups; ++k)
-          if (pw + 3 * k < kBlk / 4)
-            cp_async_16_hint(sbase + kOffKV + pos * kKVChunk + dst[k], src[k] + x * 64, nbytes[k],
-                             keep);
-        cp_async_arrive(smem_u32(&m.kv_full[pos]));
+          for (int k = 0; k < kRowGroups; ++k)
+            if (pw + 3 * k < kBlk / 4)
+              cp_async_16_hint(sbase + kOffKV + pos * kKVChunk + dst[k], src[k] + x * 64,
+                               nbytes[k], keep);
+          cp_async_arrive(smem_u32(&m.kv_full[pos]));
+        }
       }
+      ++it;
     }
     cp_async_wait_all();
   } else if (warp == 4) {
@@ -393,135 +380,168 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     if (lane == 0) {
       const uint32_t idSdP = idesc_bf16(128, 2 * kHG, false, false);  // [S^T | dP^T]
       const uint32_t idS = idesc_bf16(128, kHG, false, false);         // S^T, rope part
-      const uint32_t idQ = idesc_bf16(128, kHG, true, false);      // dQ^T: A MN-major, B K-major
-      mbar_wait(smem_u32(&m.qd_full), 0, fs, 2);
-      for (int b = 0; b < nblk; ++b) {
-        for (int i = 0; i < kCh; ++i) {
-          const int pos = pos_of_step<kRope>(i);
-          mbar_wait(smem_u32(&m.kv_full[pos]), b & 1, fs, 3);
-          fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
+      const uint32_t idQ = idesc_bf16(128, kHG, true, false);  // dQ^T: A MN-major, B K-major
+      int gb = 0, it = 0;
+      for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
+        const int t = u / G;
+        const int Kt = count[t];
+        if (Kt == 0) continue;
+        const int nblk = (Kt + kBlk - 1) / kBlk;
+        const uint32_t tdq = tmem + kColdQ + (it & 1) * kDqCols;  // this item's dQ^T buffer
+        mbar_wait(smem_u32(&m.qd_full), it & 1, fs, 2);
+        for (int b = 0; b < nblk; ++b, ++gb) {
+          for (int i = 0; i < kCh; ++i) {
+            const int pos = pos_of_step<kRope>(i);
+            mbar_wait(smem_u32(&m.kv_full[pos]), gb & 1, fs, 3);
+            fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
+            tc_fence_after();
+            const int x = dchunk_of_pos<kRope>(pos);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = sdesc_sw128(sbase + kOffKV + pos * kKVChunk + k * 32, 16, 1024);
+              // V chunks: S and dP in one N = 64 MMA (B rows: the Q heads, then
+              // the dO heads); the rope chunk adds to S only.
+              const uint64_t bqd = sdesc_sw128(sbase + kOffQD + x * kQdO + k * 32, 16, 1024);
+              umma_ss(tmem + kColS, a, bqd, x < 8 ? idSdP : idS, (i | k) != 0);
+            }
+          }
+          umma_commit(smem_u32(&m.s_full));
+          if (b == nblk - 1) umma_commit(smem_u32(&m.qd_free));  // Q / dO read for the last time
+          mbar_wait(smem_u32(&m.ds_full), gb & 1, fs, 4);
+          // the dQ^T buffer of two items ago has been read out
+          if (b == 0 && it >= 2) mbar_wait(smem_u32(&m.dq_free[it & 1]), ((it >> 1) - 1) & 1, fs, 12);
           tc_fence_after();
-          const int x = dchunk_of_pos<kRope>(pos);
+          // dQ^T chunks: rope first (its second 64-row atom reads V chunk 0 as
+          // filler rows that are never stored), then d rows 0..511.
+          for (int jj = 0; jj < kDT; ++jj) {
+            const int j = kRope ? ((jj == 0) ? 4 : jj - 1) : jj;
+            const int pos0 = (j == 4) ? 0 : (kRope ? 1 + 2 * j : 2 * j);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = sdesc_sw128(sbase + kOffKV + pos * kKVChunk + k * 32, 16, 1024);
-            // V chunks: S and dP in one N = 64 MMA (B rows: the Q heads, then the
-            // dO heads); the rope chunk adds to S only.
-            const uint64_t bqd = sdesc_sw128(sbase + kOffQD + x * kQdO + k * 32, 16, 1024);
-            umma_ss(tmem + kColS, a, bqd, x < 8 ? idSdP : idS, (i | k) != 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t a =
+                  sdesc_sw128(sbase + kOffKV + pos0 * kKVChunk + kk * 2048, kKVChunk, 1024);
+              const uint64_t bs =
+                  sdesc_sw128(sbase + kOffdS + (kk >> 2) * kHChunk + (kk & 3) * 32, 16, 1024);
+              umma_ss(tdq + j * kHG, a, bs, idQ, (b | kk) != 0);
+            }
+            if (j == 4) {
+              umma_commit(smem_u32(&m.rope_done));
+            } else {
+              umma_commit(smem_u32(&m.kv_free[pos0]));
+              umma_commit(smem_u32(&m.kv_free[pos0 + 1]));
+            }
           }
+          umma_commit(smem_u32(&m.dsp_free));
         }
-        umma_commit(smem_u32(&m.s_full));
-        mbar_wait(smem_u32(&m.ds_full), b & 1, fs, 4);
-        tc_fence_after();
-        // dQ^T chunks: rope first (its second 64-row atom reads V chunk 0 as
-        // filler rows that are never stored), then d rows 0..511.
-        for (int jj = 0; jj < kDT; ++jj) {
-          const int j = kRope ? ((jj == 0) ? 4 : jj - 1) : jj;
-          const int pos0 = (j == 4) ? 0 : (kRope ? 1 + 2 * j : 2 * j);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t a =
-                sdesc_sw128(sbase + kOffKV + pos0 * kKVChunk + kk * 2048, kKVChunk, 1024);
-            const uint64_t bs =
-                sdesc_sw128(sbase + kOffdS + (kk >> 2) * kHChunk + (kk & 3) * 32, 16, 1024);
-            umma_ss(tmem + kColdQ + j * kHG, a, bs, idQ, (b | kk) != 0);
-          }
-          if (j == 4) {
-            umma_commit(smem_u32(&m.rope_done));
-          } else {
-            umma_commit(smem_u32(&m.kv_free[pos0]));
-            umma_commit(smem_u32(&m.kv_free[pos0 + 1]));
-          }
-        }
-        umma_commit(smem_u32(&m.dsp_free));
+        umma_commit(smem_u32(&m.dq_full[it & 1]));
+        ++it;
       }
-      umma_commit(smem_u32(&m.dq_done));
-      umma_commit(smem_u32(&m.mma_done));
-      mbar_wait_final<&g_err_bwd>(smem_u32(&m.mma_done), 0);
+      if (it > 0) {  // all MMAs retired before the TMEM is freed
+        umma_commit(smem_u32(&m.mma_done));
+        mbar_wait_final<&g_err_bwd>(smem_u32(&m.mma_done), 0);
+      }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ P, dS', dq
     const float sl2 = scale * kLog2e;
     const size_t spr = static_cast<size_t>(64) * G;  // scratch rows per (token, block)
-    for (int b = 0; b < nblk; ++b) {
-      mbar_wait(smem_u32(&m.s_full), b & 1, fs, 7);
-      tc_fence_after();
-      uint32_t rs[32], rd[32];
-      tmem_ld32x2_sync(tmem + lane_base + kColS, rs, tmem + lane_base + kColdP, rd);
-      const bool valid = b * kBlk + tid < Kt;
-      float pv[kHG], dsv[kHG];
-#pragma unroll
-      for (int h = 0; h < kHG; ++h) {
-        // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
-        const float p = valid ? ex2_approx(fmaf(__uint_as_float(rs[h]), sl2, -m.lse2[h])) * m.gate[h]
-                              : 0.f;
-        pv[h] = p;
-        dsv[h] = valid ? p * (__uint_as_float(rd[h]) - m.delta[h]) * scale : 0.f;
-      }
-      if (b > 0) mbar_wait(smem_u32(&m.dsp_free), (b - 1) & 1, fs, 8);
-      // thread 0 finished reading the previous block's tiles out (bulk wait below)
-      named_bar_sync(1, 128);
-#pragma unroll
-      for (int h = 0; h < kHG; ++h) {
-        const __nv_bfloat16 v = __float2bfloat16_rn(dsv[h]);
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(sbase + kOffdS + hs_tile_off(h, tid)),
-                     "h"(*reinterpret_cast<const unsigned short*>(&v))
-                     : "memory");
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&m.ds_full));
-      // With a rope chunk, P goes into position 0 once the rope part of dQ has
-      // read the rope rows.
-      if constexpr (kRope) mbar_wait(smem_u32(&m.rope_done), b & 1, fs, 9);
-#pragma unroll
-      for (int h = 0; h < kHG; ++h) {
-        const __nv_bfloat16 v = __float2bfloat16_rn(pv[h]);
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(sbase + kOffP + hs_tile_off(h, tid)),
-                     "h"(*reinterpret_cast<const unsigned short*>(&v))
-                     : "memory");
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (tid == 0) {
-        // dS' and P rows of this head group -> the (token, block) scratch tile
-        const int row0 = static_cast<int>((static_cast<size_t>(t) * nbmax + b) * spr) + h0;
-        const uint64_t pol = l2_evict_first();
-        for (int half = 0; half < 2; ++half) {
-          tma_store_2d_hint(&tm_sp, half * 64, row0, sbase + kOffdS + half * kHChunk, pol);
-          tma_store_2d_hint(&tm_sp, half * 64, row0 + 32 * G, sbase + kOffP + half * kHChunk, pol);
+    int gb = 0, it = 0;
+    for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
+      const int t = u / G, h0 = (u - t * G) * kHG;
+      const int nh = min(kHG, H - h0);
+      const int Kt = count[t];
+      if (Kt == 0) {  // empty row: dq = 0, nothing for dkv
+        for (int v = tid; v < nh * (kD / 8); v += 128) {
+          const int h = v / (kD / 8), c = v - h * (kD / 8);
+          *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kD + c * 8) =
+              make_uint4(0, 0, 0, 0);
         }
-        bulk_commit();
-        bulk_wait_read();
-        if constexpr (kRope) mbar_arrive(smem_u32(&m.kv_free[0]));  // position 0 may take the next rope rows
+        continue;
       }
-    }
-
-    // dQ^T -> dq (bf16), staged through shared memory for one bulk store.
-    // With a rope chunk the staging area overlaps the last P tile: thread 0
-    // reaches this barrier only after that tile's store has been read out.
-    named_bar_sync(1, 128);
-    mbar_wait(smem_u32(&m.dq_done), 0, fs, 10);
-    tc_fence_after();
-    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV);  // [32][kD]
-    for (int j = 0; j < kDT; ++j) {
-      uint32_t v[32];
-      tmem_ld32_sync(tmem + lane_base + kColdQ + j * kHG, v);
-      const int d = j * 128 + tid;
-      if (d < kD) {
+      const int nblk = (Kt + kBlk - 1) / kBlk;
+      if (tid < kHG) {
+        // Padded heads get gate 0, hence P = dS = 0: they add nothing anywhere.
+        const bool real = tid < nh;
+        const size_t r = static_cast<size_t>(t) * H + h0 + tid;
+        m.lse2[tid] = real ? lse2_g[r] : 0.f;
+        m.gate[tid] = real ? gate_g[r] : 0.f;
+        m.delta[tid] = real ? delta_g[r] : 0.f;
+      }
+      named_bar_sync(1, 128);
+      for (int b = 0; b < nblk; ++b, ++gb) {
+        mbar_wait(smem_u32(&m.s_full), gb & 1, fs, 7);
+        tc_fence_after();
+        uint32_t rs[32], rd[32];
+        tmem_ld32x2_sync(tmem + lane_base + kColS, rs, tmem + lane_base + kColdP, rd);
+        const bool valid = b * kBlk + tid < Kt;
+        float pv[kHG], dsv[kHG];
 #pragma unroll
-        for (int h = 0; h < kHG; ++h) stage[h * kD + d] = __float2bfloat16_rn(__uint_as_float(v[h]));
+        for (int h = 0; h < kHG; ++h) {
+          // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
+          const float p =
+              valid ? ex2_approx(fmaf(__uint_as_float(rs[h]), sl2, -m.lse2[h])) * m.gate[h] : 0.f;
+          pv[h] = p;
+          dsv[h] = valid ? p * (__uint_as_float(rd[h]) - m.delta[h]) * scale : 0.f;
+        }
+        if (gb > 0) mbar_wait(smem_u32(&m.dsp_free), (gb - 1) & 1, fs, 8);
+        // thread 0 finished reading the previous block's tiles out (bulk wait below)
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int h = 0; h < kHG; ++h) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(dsv[h]);
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(sbase + kOffdS + hs_tile_off(h, tid)),
+                       "h"(*reinterpret_cast<const unsigned short*>(&v))
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&m.ds_full));
+        // With a rope chunk, P goes into position 0 once the rope part of dQ
+        // has read the rope rows.
+        if constexpr (kRope) mbar_wait(smem_u32(&m.rope_done), gb & 1, fs, 9);
+#pragma unroll
+        for (int h = 0; h < kHG; ++h) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(pv[h]);
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(sbase + kOffP + hs_tile_off(h, tid)),
+                       "h"(*reinterpret_cast<const unsigned short*>(&v))
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (tid == 0) {
+          // dS' and P rows of this head group -> the (token, block) scratch tile
+          const int row0 = static_cast<int>((static_cast<size_t>(t) * nbmax + b) * spr) + h0;
+          const uint64_t pol = l2_evict_first();
+          for (int half = 0; half < 2; ++half) {
+            tma_store_2d_hint(&tm_sp, half * 64, row0, sbase + kOffdS + half * kHChunk, pol);
+            tma_store_2d_hint(&tm_sp, half * 64, row0 + 32 * G, sbase + kOffP + half * kHChunk,
+                              pol);
+          }
+          bulk_commit();
+          bulk_wait_read();
+          if constexpr (kRope) mbar_arrive(smem_u32(&m.kv_free[0]));  // position 0 may take the next rope rows
+        }
       }
-    }
-    fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (tid == 0) {  // dq rows (t, h0..h0+nh) are contiguous
-      bulk_store_hint(dq + (static_cast<size_t>(t) * H + h0) * kD, smem_u32(stage),
-                      nh * kD * 2, l2_evict_first());
-      bulk_commit();
-      bulk_wait_read();
+      // dQ^T -> dq (bf16), straight from registers: for each head, a warp
+      // writes 32 consecutive d of that head's row.
+      mbar_wait(smem_u32(&m.dq_full[it & 1]), (it >> 1) & 1, fs, 10);
+      tc_fence_after();
+      const uint32_t tdq = tmem + lane_base + kColdQ + (it & 1) * kDqCols;
+      __nv_bfloat16* dq_t = dq + (static_cast<size_t>(t) * H + h0) * kD;
+      for (int j = 0; j < kDT; ++j) {
+        uint32_t v[32];
+        tmem_ld32_sync(tdq + j * kHG, v);
+        const int d = j * 128 + tid;
+        if (d < kD) {
+#pragma unroll
+          for (int h = 0; h < kHG; ++h)
+            if (h < nh) dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(__uint_as_float(v[h]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&m.dq_free[it & 1]));
+      ++it;
     }
   }
 
@@ -811,6 +831,15 @@ k_dsink(const float* __restrict__ dsink_t, float* __restrict__ dsink, int T, int
   if (threadIdx.x == 0) dsink[h] = red[0];
 }
 
+// SMs of the current device (the persistent grid size).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
 }  // namespace
 
 cudaError_t launch_compact(const Problem& p, const int32_t* idx, const int32_t* len,
@@ -880,7 +909,10 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     if (e != cudaSuccess) return e;
     auto kern = p.d_qk == 512 ? k_bwd_dq<512> : k_bwd_dq<576>;
     const int smem = p.d_qk == 512 ? DqLayout<512>::kSmemBytes : DqLayout<576>::kSmemBytes;
-    kern<<<static_cast<unsigned>(static_cast<long long>(p.T) * G), kThreads, smem, s>>>(
+    // persistent: at most one CTA per SM, each walking its share of the items
+    const long long items = static_cast<long long>(p.T) * G;
+    const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
+    kern<<<grid, kThreads, smem, s>>>(
         tm_q, tm_do, tm_sp_st, tm_kv, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2,
         gate,
         delta, static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, box_heads, nbmax);
