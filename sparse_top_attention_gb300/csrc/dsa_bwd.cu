@@ -831,15 +831,6 @@ k_dsink(const float* __restrict__ dsink_t, float* __restrict__ dsink, int T, int
   if (threadIdx.x == 0) dsink[h] = red[0];
 }
 
-// SMs of the current device (the persistent grid size).
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-    return 1;
-  return n;
-}
-
 }  // namespace
 
 cudaError_t launch_compact(const Problem& p, const int32_t* idx, const int32_t* len,

@@ -109,10 +109,14 @@ __device__ __forceinline__ void load_index_row(const int32_t* __restrict__ idx_r
   }
 }
 
+// Compacts a register-held index row (element i * nthreads + tid in vals[i])
+// with `nthreads` threads (whole warps, thread ids 0..nthreads-1 within the
+// group) that synchronise on named barrier `bar`.
 template <int kN>
 __device__ __forceinline__ int compact_token_regs(const int32_t (&vals)[kN], int W, int len,
                                                   KvRange kv, int32_t* list, int cap,
-                                                  int* warp_counts, int tid, int nthreads) {
+                                                  int* warp_counts, int tid, int nthreads,
+                                                  int bar) {
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
   int base = 0;
@@ -124,7 +128,7 @@ __device__ __forceinline__ int compact_token_regs(const int32_t (&vals)[kN], int
     const bool ok = j < W && slot_valid(v, j, len, kv.n);
     const unsigned bal = __ballot_sync(0xffffffffu, ok);
     if (lane == 0) warp_counts[warp] = __popc(bal);
-    __syncthreads();
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthreads) : "memory");
     int off = base, tot = 0;
     for (int w = 0; w < nwarps; ++w) {
       const int c = warp_counts[w];
@@ -134,9 +138,29 @@ __device__ __forceinline__ int compact_token_regs(const int32_t (&vals)[kN], int
     const int pos = off + __popc(bal & lt_mask);
     if (ok && pos < cap) list[pos] = kv.lo + v;
     base += tot;
-    __syncthreads();
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthreads) : "memory");
   }
   return base;
+}
+
+// Number of valid slots of one index row, counted by one warp (every lane
+// gets the count).  The same rule as the compaction: slot j < min(len, W)
+// holding an index in [0, kv.n).
+__device__ __forceinline__ int warp_count_valid(const int32_t* __restrict__ idx_row, int W,
+                                                int len, KvRange kv, int lane) {
+  const int lim = len < W ? len : W;
+  int n = 0;
+  for (int j0 = 0; j0 < lim; j0 += 128) {
+    int32_t v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q * 32 + lane;
+      v[q] = j < lim ? idx_row[j] : -1;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) n += __popc(__ballot_sync(0xffffffffu, v[q] >= 0 && v[q] < kv.n));
+  }
+  return n;
 }
 
 }  // namespace dsa

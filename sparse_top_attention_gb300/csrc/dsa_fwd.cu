@@ -47,6 +47,7 @@ constexpr int kQIssuer = 160;               // lane 0 of warp 5
 constexpr int kProducers = 96;              // warps 5-7
 constexpr int kQChunk = kHG * 128;           // one 64-column chunk of Q: 8 KB
 constexpr int kKVChunk = kBlk * 128;         // one 64-column chunk of 128 rows: 16 KB
+constexpr int kIdxRegs = (kMaxW + kProducers - 1) / kProducers;  // index row per producer
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
@@ -56,7 +57,7 @@ constexpr uint32_t kColO = 64;    // O^T: 4 chunks x 64 columns
 struct Misc {
   uint64_t kv_full[kChunks];
   uint64_t kv_free[kChunks];
-  uint64_t q_full, s_full, p_full, o_done, mma_done;
+  uint64_t q_full, q_free, s_full, p_full, o_done, mma_done;
   float red[2][4][kHG];   // per-warp column maxima, double-buffered by block parity
   float m_used[kHG];      // running shift per head (log2 units)
   float fac[kHG];         // rescale factor per head, then the output scale
@@ -113,9 +114,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                 kOffP = L::kOffP, kOffMisc = L::kOffMisc;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t = blockIdx.x / G, grp = blockIdx.x - t * G;
-  const int h0 = grp * kHG;
-  const int nh = min(kHG, H - h0);
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // uniform across the CTA; never expected
     if (tid == 0) atomicCAS(&g_err_fwd, 0u, 0x2FFu);
@@ -124,29 +122,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
   int32_t* list = reinterpret_cast<int32_t*>(smem + kOffList);
   const FailState fs{&g_err_fwd, &m.abort_flag};
-
-  // The Q tile of the head group (kCh chunks of [box_heads x 64 columns],
-  // 128B swizzle; heads past H inside the box are zero-filled by the TMA)
-  // loads from kernel entry: its issuing thread owns its barrier.  The
-  // token's index row is read into registers now as well, so that both
-  // latencies overlap the set-up below.
-  if (tid == kQIssuer) {
-    mbar_init(smem_u32(&m.q_full), 1);
-    mbar_init_fence();
-    mbar_arrive_expect_tx(smem_u32(&m.q_full), kCh * box_heads * 128);
-    const uint64_t pol = l2_evict_first();
-    for (int c = 0; c < kCh; ++c)
-      tma_load_3d_hint(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t, smem_u32(&m.q_full),
-                       pol);
-  }
-  int32_t idx_regs[kMaxW / kThreads];
-  load_index_row(topk_idxs + static_cast<size_t>(t) * W, W, tid, kThreads, idx_regs);
+  // Persistent: CTA c takes items c, c + gridDim.x, ... of the (token, head
+  // group) list.  Every role walks the same items and finds each item's
+  // valid-slot count itself; barrier phases follow running counts of
+  // non-empty items (Q tile) and of blocks (everything else).
+  const int n_items = T * G;
+  const size_t lo_off = residual ? static_cast<size_t>(T) * H * kDv : 0;  // residual half
 
   if (tid == 0) {
     for (int c = 0; c < kCh; ++c) {
       mbar_init(smem_u32(&m.kv_full[c]), kProducers);
       mbar_init(smem_u32(&m.kv_free[c]), 1);
     }
+    mbar_init(smem_u32(&m.q_full), 1);
+    mbar_init(smem_u32(&m.q_free), 1);
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.p_full), 128);
     mbar_init(smem_u32(&m.o_done), 1);
@@ -155,7 +144,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     mbar_init_fence();
   }
   if (tid < kHG) m.m_used[tid] = -INFINITY;
-  // Q tile rows that the TMA box does not cover (only when H < 64) are zero.
+  // Q tile rows that the TMA box does not cover (only when H < 64) are zero;
+  // the loads never write them, so once is enough.
   for (int i = tid; i < kCh * (kHG - box_heads) * 8; i += kThreads) {
     const int per = (kHG - box_heads) * 8;
     const int c = i / per, rem = i - c * per;
@@ -166,29 +156,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                  : "memory");
   }
   fence_proxy_async_smem();
-  __syncthreads();
-
-  // a1: decode and compact the valid slots of token t (slot order).
-  const int len = slot_len(topk_length, t, W);
-  const KvRange kvr = kv_range(cu_q, cu_kv, B, t, S_kv);
-  const int Kt = compact_token_regs(idx_regs, W, len, kvr, list, kMaxW, m.warp_counts, tid,
-                                    kThreads);
-
-  const size_t lo_off = residual ? static_cast<size_t>(T) * H * kDv : 0;  // residual half
-  if (Kt == 0) {  // empty row: out = 0, lse = -FLT_MAX, no tensor-core work
-    for (int v = tid; v < nh * (kDv / 8); v += kThreads) {
-      const int h = v / (kDv / 8), c = v - h * (kDv / 8);
-      const size_t o = (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8;
-      *reinterpret_cast<uint4*>(out + o) = make_uint4(0, 0, 0, 0);
-      if (residual) *reinterpret_cast<uint4*>(out + lo_off + o) = make_uint4(0, 0, 0, 0);
-    }
-    if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = -kFltMax;
-    // the Q tile is still landing in this CTA's shared memory: let it finish
-    if (tid == kQIssuer) mbar_wait_final(smem_u32(&m.q_full), 0);
-    return;
-  }
-  const int nblk = (Kt + kBlk - 1) / kBlk;
-
   if (warp == 4) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -197,94 +164,134 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
   if (warp >= 5) {
     // ------------------------------------------------------------ gather
-    // cp.async 16-byte pieces into the 128B-swizzled chunk tiles; one warp
-    // instruction moves 4 whole 128-byte row pieces.  Rows past the valid
-    // count are zero-filled (their scores are masked).
-    const int pw = warp - 5;
+    // Per item: compact the token's valid slots into the row list (slot
+    // order), load the Q tile of the head group by TMA once the previous
+    // item's S GEMMs are done with it, then gather the rows block by block:
+    // cp.async 16-byte pieces into the 128B-swizzled chunk tiles (one warp
+    // instruction moves 4 whole 128-byte row pieces; rows past the valid
+    // count are zero-filled and their scores masked), or one 2-D TMA load
+    // per chunk for a block of consecutive rows (the sliding window).
+    const int ptid = tid - kQIssuer, pw = warp - 5;
     const uint64_t keep = l2_evict_last();
-    for (int b = 0; b < nblk; ++b) {
-      // This lane's rows of the block, read once (before the wait on the
-      // first chunk, so the reads overlap it) and reused by all 9 chunks.
-      const __nv_bfloat16* src[kRowGroups];
-      uint32_t dst[kRowGroups], nbytes[kRowGroups];
+    int it = 0, gb = 0;  // non-empty items and blocks so far
+    for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
+      const int t = u / G, h0 = (u - t * G) * kHG;
+      int32_t idx_regs[kIdxRegs];
+      load_index_row(topk_idxs + static_cast<size_t>(t) * W, W, ptid, kProducers, idx_regs);
+      // Every producer has issued the previous item's last gathers (the
+      // list reads) before the first barrier inside, ahead of any write.
+      const int Kt = compact_token_regs(idx_regs, W, slot_len(topk_length, t, W),
+                                        kv_range(cu_q, cu_kv, B, t, S_kv), list, kMaxW,
+                                        m.warp_counts, ptid, kProducers, 2);
+      if (Kt == 0) continue;
+      const int nblk = (Kt + kBlk - 1) / kBlk;
+      if (tid == kQIssuer) {
+        if (it > 0) mbar_wait(smem_u32(&m.q_free), (it - 1) & 1, fs, 8);
+        mbar_arrive_expect_tx(smem_u32(&m.q_full), kCh * box_heads * 128);
+        const uint64_t pol = l2_evict_first();
+        for (int c = 0; c < kCh; ++c)
+          tma_load_3d_hint(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t,
+                           smem_u32(&m.q_full), pol);
+      }
+      for (int b = 0; b < nblk; ++b, ++gb) {
+        // This lane's rows of the block, read once (before the wait on the
+        // first chunk, so the reads overlap it) and reused by all chunks.
+        const __nv_bfloat16* src[kRowGroups];
+        uint32_t dst[kRowGroups], nbytes[kRowGroups];
 #pragma unroll
-      for (int k = 0; k < kRowGroups; ++k) {
-        const int g = pw + 3 * k;
-        const int row = g * 4 + (lane >> 3), pc = lane & 7;
-        const int slot = b * kBlk + row;
-        const bool ok = g < kBlk / 4 && slot < Kt;
-        const int r = ok ? list[slot] : 0;
-        src[k] = kv + static_cast<size_t>(r) * kD + pc * 8;
-        dst[k] = sw128_off(row & (kBlk - 1), pc);
-        nbytes[k] = ok ? 16u : 0u;
-      }
-      // A full block of consecutive KV rows (the sliding window) comes in with
-      // one 2-D TMA load per chunk instead of 128 row copies.
-      bool contig = false;
-      int r0 = 0;
-      if (b * kBlk + kBlk <= Kt) {
-        r0 = list[b * kBlk];
-        bool mine = true;
-        for (int i = tid - kQIssuer; i < kBlk; i += kProducers) mine &= list[b * kBlk + i] == r0 + i;
-        contig = !named_bar_or(2, kProducers, !mine);
-      }
-      for (int c = 0; c < kCh; ++c) {
-        if (b > 0) mbar_wait(smem_u32(&m.kv_free[c]), (b - 1) & 1, fs, 1);
-        if (contig) {
-          if (tid == kQIssuer) {
-            mbar_arrive_expect_tx(smem_u32(&m.kv_full[c]), kKVChunk);
-            tma_load_2d_hint(sbase + kOffKV + c * kKVChunk, &tm_kv, c * 64, r0,
-                             smem_u32(&m.kv_full[c]), keep);
-          } else {
-            mbar_arrive(smem_u32(&m.kv_full[c]));
-          }
-          continue;
+        for (int k = 0; k < kRowGroups; ++k) {
+          const int g = pw + 3 * k;
+          const int row = g * 4 + (lane >> 3), pc = lane & 7;
+          const int slot = b * kBlk + row;
+          const bool ok = g < kBlk / 4 && slot < Kt;
+          const int r = ok ? list[slot] : 0;
+          src[k] = kv + static_cast<size_t>(r) * kD + pc * 8;
+          dst[k] = sw128_off(row & (kBlk - 1), pc);
+          nbytes[k] = ok ? 16u : 0u;
         }
+        bool contig = false;
+        int r0 = 0;
+        if (b * kBlk + kBlk <= Kt) {
+          r0 = list[b * kBlk];
+          bool mine = true;
+          for (int i = ptid; i < kBlk; i += kProducers) mine &= list[b * kBlk + i] == r0 + i;
+          contig = !named_bar_or(2, kProducers, !mine);
+        }
+        for (int c = 0; c < kCh; ++c) {
+          if (gb > 0) mbar_wait(smem_u32(&m.kv_free[c]), (gb - 1) & 1, fs, 1);
+          if (contig) {
+            if (tid == kQIssuer) {
+              mbar_arrive_expect_tx(smem_u32(&m.kv_full[c]), kKVChunk);
+              tma_load_2d_hint(sbase + kOffKV + c * kKVChunk, &tm_kv, c * 64, r0,
+                               smem_u32(&m.kv_full[c]), keep);
+            } else {
+              mbar_arrive(smem_u32(&m.kv_full[c]));
+            }
+            continue;
+          }
 #pragma unroll
-        for (int k = 0; k < kRowGroups; ++k)
-          if (pw + 3 * k < kBlk / 4)
-            cp_async_16_hint(sbase + kOffKV + c * kKVChunk + dst[k], src[k] + c * 64, nbytes[k],
-                             keep);
-        cp_async_arrive(smem_u32(&m.kv_full[c]));
+          for (int k = 0; k < kRowGroups; ++k)
+            if (pw + 3 * k < kBlk / 4)
+              cp_async_16_hint(sbase + kOffKV + c * kKVChunk + dst[k], src[k] + c * 64,
+                               nbytes[k], keep);
+          cp_async_arrive(smem_u32(&m.kv_full[c]));
+        }
       }
+      ++it;
     }
     cp_async_wait_all();
   } else if (warp == 4) {
     // ------------------------------------------------------------ UMMA issue
-    if (lane == 0) {
-      const uint32_t idS = idesc_bf16(128, kHG, false, false);
-      const uint32_t idPV = idesc_bf16(128, kHG, true, true);
-      const uint32_t tS = tmem + kColS, tO = tmem + kColO;
-      mbar_wait(smem_u32(&m.q_full), 0, fs, 2);
-      for (int b = 0; b < nblk; ++b) {
-        for (int c = 0; c < kCh; ++c) {
-          mbar_wait(smem_u32(&m.kv_full[c]), b & 1, fs, 3);
-          fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
+    const uint32_t idS = idesc_bf16(128, kHG, false, false);
+    const uint32_t idPV = idesc_bf16(128, kHG, true, true);
+    const uint32_t tS = tmem + kColS, tO = tmem + kColO;
+    int it = 0, gb = 0;
+    for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
+      const int t = u / G;
+      const int Kt = warp_count_valid(topk_idxs + static_cast<size_t>(t) * W, W,
+                                      slot_len(topk_length, t, W),
+                                      kv_range(cu_q, cu_kv, B, t, S_kv), lane);
+      if (Kt == 0) continue;
+      const int nblk = (Kt + kBlk - 1) / kBlk;
+      if (lane == 0) {
+        mbar_wait(smem_u32(&m.q_full), it & 1, fs, 2);
+        for (int b = 0; b < nblk; ++b) {
+          const int g = gb + b;
+          for (int c = 0; c < kCh; ++c) {
+            mbar_wait(smem_u32(&m.kv_full[c]), g & 1, fs, 3);
+            fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = sdesc_sw128(sbase + kOffKV + c * kKVChunk + k * 32, 16, 1024);
+              const uint64_t bq = sdesc_sw128(sbase + kOffQ + c * kQChunk + k * 32, 16, 1024);
+              umma_ss(tS, a, bq, idS, (c | k) != 0);
+            }
+          }
+          umma_commit(smem_u32(&m.s_full));
+          if (b == nblk - 1) umma_commit(smem_u32(&m.q_free));  // Q read for the last time
+          mbar_wait(smem_u32(&m.p_full), g & 1, fs, 4);
           tc_fence_after();
+          for (int j = 0; j < 4; ++j) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t a = sdesc_sw128(sbase + kOffKV + c * kKVChunk + k * 32, 16, 1024);
-            const uint64_t bq = sdesc_sw128(sbase + kOffQ + c * kQChunk + k * 32, 16, 1024);
-            umma_ss(tS, a, bq, idS, (c | k) != 0);
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t a =
+                  sdesc_sw128(sbase + kOffKV + (2 * j) * kKVChunk + k * 2048, kKVChunk, 1024);
+              const uint64_t bp = sdesc_sw128(sbase + kOffP + k * 2048, kKVChunk, 1024);
+              umma_ss(tO + j * kHG, a, bp, idPV, (b | k) != 0);
+            }
+            umma_commit(smem_u32(&m.kv_free[2 * j]));
+            umma_commit(smem_u32(&m.kv_free[2 * j + 1]));
           }
+          if constexpr (L::kRope) umma_commit(smem_u32(&m.kv_free[8]));
+          umma_commit(smem_u32(&m.o_done));
         }
-        umma_commit(smem_u32(&m.s_full));
-        mbar_wait(smem_u32(&m.p_full), b & 1, fs, 4);
-        tc_fence_after();
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t a =
-                sdesc_sw128(sbase + kOffKV + (2 * j) * kKVChunk + k * 2048, kKVChunk, 1024);
-            const uint64_t bp = sdesc_sw128(sbase + kOffP + k * 2048, kKVChunk, 1024);
-            umma_ss(tO + j * kHG, a, bp, idPV, (b | k) != 0);
-          }
-          umma_commit(smem_u32(&m.kv_free[2 * j]));
-          umma_commit(smem_u32(&m.kv_free[2 * j + 1]));
-        }
-        if constexpr (L::kRope) umma_commit(smem_u32(&m.kv_free[8]));
-        umma_commit(smem_u32(&m.o_done));
       }
+      gb += nblk;
+      ++it;
+      __syncwarp();
+    }
+    if (lane == 0 && it > 0) {  // all MMAs retired before the TMEM is freed
       umma_commit(smem_u32(&m.mma_done));
       mbar_wait_final(smem_u32(&m.mma_done), 0);
     }
@@ -294,144 +301,167 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const float sl2 = scale * kLog2e;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tS_row = tmem + lane_base + kColS;
-    float lp[kHG];
+    int gb = 0;
+    for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
+      const int t = u / G, h0 = (u - t * G) * kHG;
+      const int nh = min(kHG, H - h0);
+      const int Kt = warp_count_valid(topk_idxs + static_cast<size_t>(t) * W, W,
+                                      slot_len(topk_length, t, W),
+                                      kv_range(cu_q, cu_kv, B, t, S_kv), lane);
+      if (Kt == 0) {  // empty row: out = 0, lse = -FLT_MAX, no tensor-core work
+        for (int v = tid; v < nh * (kDv / 8); v += 128) {
+          const int h = v / (kDv / 8), c = v - h * (kDv / 8);
+          const size_t o = (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8;
+          *reinterpret_cast<uint4*>(out + o) = make_uint4(0, 0, 0, 0);
+          if (residual) *reinterpret_cast<uint4*>(out + lo_off + o) = make_uint4(0, 0, 0, 0);
+        }
+        if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = -kFltMax;
+        continue;
+      }
+      const int nblk = (Kt + kBlk - 1) / kBlk;
+      float lp[kHG];
 #pragma unroll
-    for (int h = 0; h < kHG; ++h) lp[h] = 0.f;
-    __nv_bfloat16* const sP = reinterpret_cast<__nv_bfloat16*>(smem + kOffP);
-    (void)sP;
+      for (int h = 0; h < kHG; ++h) lp[h] = 0.f;
 
-    for (int b = 0; b < nblk; ++b) {
-      mbar_wait(smem_u32(&m.s_full), b & 1, fs, 5);
-      tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld32x2_sync(tS_row, r0, tS_row + 32, r1);
-      const bool valid = b * kBlk + tid < Kt;
-      float s[kHG];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        s[i] = valid ? __uint_as_float(r0[i]) * sl2 : -INFINITY;
-        s[32 + i] = valid ? __uint_as_float(r1[i]) * sl2 : -INFINITY;
-      }
-      // Lazy rescale: a head keeps its shift unless the block's maximum
-      // exceeds it by more than 2^8; the final normalisation uses the same
-      // shift for O and l.  The column maxima are only needed when some score
-      // is that far above its head's shift (always in the first block), so
-      // one vote decides whether to compute them.
-      bool above = false;
-#pragma unroll
-      for (int h = 0; h < kHG; ++h) above |= s[h] > m.m_used[h] + 8.f;
-      bool any = named_bar_or(1, 128, above);
-      if (any) {
-        // column (per-head) maximum over the 128 gathered rows
-        float* red = m.red[b & 1][warp];
-#pragma unroll
-        for (int h = 0; h < kHG; ++h) {
-          const float mx = warp_max(s[h]);
-          if ((h & 31) == lane) red[h] = mx;
-        }
-        named_bar_sync(1, 128);
-        bool resc = false;
-        if (tid < kHG) {
-          const float bm = fmaxf(fmaxf(m.red[b & 1][0][tid], m.red[b & 1][1][tid]),
-                                 fmaxf(m.red[b & 1][2][tid], m.red[b & 1][3][tid]));
-          const float mo = m.m_used[tid];
-          const float mn = fmaxf(mo, bm);
-          resc = mn > mo + 8.f;
-          m.fac[tid] = resc ? ex2_approx(mo - mn) : 1.f;
-          if (resc) m.m_used[tid] = mn;
-        }
-        any = named_bar_or(1, 128, resc);
-      }
-      if (any) {
-#pragma unroll
-        for (int h = 0; h < kHG; ++h) lp[h] *= m.fac[h];
-      }
-      // P^T row as bf16 pairs; s[] is dead after this loop.
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2_approx(s[2 * i] - m.m_used[2 * i]);
-        const float p1 = ex2_approx(s[2 * i + 1] - m.m_used[2 * i + 1]);
-        lp[2 * i] += p0;
-        lp[2 * i + 1] += p1;
-        pk[i] = pack_bf16x2(p0, p1);
-      }
-      if (any && b > 0) {
-        // O^T columns of heads whose shift moved: scale by 2^(old - new).
-        mbar_wait(smem_u32(&m.o_done), (b - 1) & 1, fs, 6);
+      for (int b = 0; b < nblk; ++b) {
+        const int g = gb + b;
+        mbar_wait(smem_u32(&m.s_full), g & 1, fs, 5);
         tc_fence_after();
-        for (int j = 0; j < 4; ++j) {
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t ta = tmem + lane_base + kColO + j * kHG + half * 32;
-            uint32_t r[32];
-            tmem_ld32_sync(ta, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              r[i] = __float_as_uint(__uint_as_float(r[i]) * m.fac[half * 32 + i]);
-            tmem_st32(ta, r);
-          }
-        }
-        tmem_wait_st();
-      }
-      // Store into the swizzled MN-major tile that the PV UMMA reads.
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t dst = sbase + kOffP + sw128_off(tid, c);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
-                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&m.p_full));
-    }
-
-    // ------------------------------------------------------------ epilogue
-    mbar_wait(smem_u32(&m.o_done), (nblk - 1) & 1, fs, 7);
-    tc_fence_after();
-    float* lbuf = reinterpret_cast<float*>(smem + kOffKV);  // [128][65]
-#pragma unroll
-    for (int h = 0; h < kHG; ++h) lbuf[tid * 65 + h] = lp[h];
-    named_bar_sync(1, 128);
-    if (tid < kHG) {
-      float l = 0.f;
-      for (int r = 0; r < kBlk; ++r) l += lbuf[r * 65 + tid];
-      const float lse_nat = (m.m_used[tid] + log2f(l)) * kLn2;
-      const float sk = (sink != nullptr && tid < nh) ? sink[h0 + tid] : -INFINITY;
-      const float gate = stable_sigmoid(lse_nat - sk);
-      m.fac[tid] = gate / l;
-      if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = lse_nat;
-    }
-    named_bar_sync(1, 128);
-    // Stage bf16 rows [64][512] (and their rounding residual) over the free KV
-    // tiles; the l partials there were consumed before the barrier above.
-    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV);
-    __nv_bfloat16* stage_lo = reinterpret_cast<__nv_bfloat16*>(smem + kOffKV + kHG * kDv * 2);
-    for (int j = 0; j < 4; ++j) {
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32_sync(tmem + lane_base + kColO + j * kHG + half * 32, r);
-        const int d = j * 128 + tid;
+        uint32_t r0[32], r1[32];
+        tmem_ld32x2_sync(tS_row, r0, tS_row + 32, r1);
+        const bool valid = b * kBlk + tid < Kt;
+        float s[kHG];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int h = half * 32 + i;
-          const float o = __uint_as_float(r[i]) * m.fac[h];
-          const __nv_bfloat16 hi = __float2bfloat16_rn(o);
-          stage[h * kDv + d] = hi;
-          if (residual) stage_lo[h * kDv + d] = __float2bfloat16_rn(o - __bfloat162float(hi));
+          s[i] = valid ? __uint_as_float(r0[i]) * sl2 : -INFINITY;
+          s[32 + i] = valid ? __uint_as_float(r1[i]) * sl2 : -INFINITY;
+        }
+        // Lazy rescale: a head keeps its shift unless the block's maximum
+        // exceeds it by more than 2^8; the final normalisation uses the same
+        // shift for O and l.  The column maxima are only needed when some
+        // score is that far above its head's shift (always in the first
+        // block), so one vote decides whether to compute them.
+        bool above = false;
+#pragma unroll
+        for (int h = 0; h < kHG; ++h) above |= s[h] > m.m_used[h] + 8.f;
+        bool any = named_bar_or(1, 128, above);
+        if (any) {
+          // column (per-head) maximum over the 128 gathered rows
+          float* red = m.red[g & 1][warp];
+#pragma unroll
+          for (int h = 0; h < kHG; ++h) {
+            const float mx = warp_max(s[h]);
+            if ((h & 31) == lane) red[h] = mx;
+          }
+          named_bar_sync(1, 128);
+          bool resc = false;
+          if (tid < kHG) {
+            const float bm = fmaxf(fmaxf(m.red[g & 1][0][tid], m.red[g & 1][1][tid]),
+                                   fmaxf(m.red[g & 1][2][tid], m.red[g & 1][3][tid]));
+            const float mo = m.m_used[tid];
+            const float mn = fmaxf(mo, bm);
+            resc = mn > mo + 8.f;
+            m.fac[tid] = resc ? ex2_approx(mo - mn) : 1.f;
+            if (resc) m.m_used[tid] = mn;
+          }
+          any = named_bar_or(1, 128, resc);
+        }
+        if (any) {
+#pragma unroll
+          for (int h = 0; h < kHG; ++h) lp[h] *= m.fac[h];
+        }
+        // P^T row as bf16 pairs; s[] is dead after this loop.
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(s[2 * i] - m.m_used[2 * i]);
+          const float p1 = ex2_approx(s[2 * i + 1] - m.m_used[2 * i + 1]);
+          lp[2 * i] += p0;
+          lp[2 * i + 1] += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        if (any && b > 0) {
+          // O^T columns of heads whose shift moved: scale by 2^(old - new).
+          mbar_wait(smem_u32(&m.o_done), (g - 1) & 1, fs, 6);
+          tc_fence_after();
+          for (int j = 0; j < 4; ++j) {
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t ta = tmem + lane_base + kColO + j * kHG + half * 32;
+              uint32_t r[32];
+              tmem_ld32_sync(ta, r);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                r[i] = __float_as_uint(__uint_as_float(r[i]) * m.fac[half * 32 + i]);
+              tmem_st32(ta, r);
+            }
+          }
+          tmem_wait_st();
+        }
+        // Store into the swizzled MN-major tile that the PV UMMA reads.
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t dst = sbase + kOffP + sw128_off(tid, c);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
+                       "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&m.p_full));
+      }
+      gb += nblk;
+
+      // ---------------------------------------------------------- epilogue
+      // l per head: a butterfly reduce-scatter leaves lane L of each warp
+      // with its warp's sums for heads 2L and 2L + 1 in lp[0..1]; the four
+      // warps' partials meet in shared memory (both halves of red are free:
+      // the block loop's last barrier came after their last reads).
+#pragma unroll
+      for (int o = 16, n = 32; o > 0; o >>= 1, n >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+          const float keep = up ? lp[i + n] : lp[i];
+          const float send = up ? lp[i] : lp[i + n];
+          lp[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
       }
-    }
-    fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (tid == 0) {
-      // out rows (t, h0..h0+nh) are contiguous: one bulk store per half
-      const size_t o = (static_cast<size_t>(t) * H + h0) * kDv;
-      const uint64_t pol = l2_evict_first();
-      bulk_store_hint(out + o, smem_u32(stage), nh * kDv * 2, pol);
-      if (residual) bulk_store_hint(out + lo_off + o, smem_u32(stage_lo), nh * kDv * 2, pol);
-      bulk_commit();
-      bulk_wait_read();
+      *reinterpret_cast<float2*>(&m.red[0][warp][2 * lane]) = make_float2(lp[0], lp[1]);
+      named_bar_sync(1, 128);
+      if (tid < kHG) {
+        const float l = (m.red[0][0][tid] + m.red[0][1][tid]) + (m.red[0][2][tid] + m.red[0][3][tid]);
+        const float lse_nat = (m.m_used[tid] + log2f(l)) * kLn2;
+        const float sk = (sink != nullptr && tid < nh) ? sink[h0 + tid] : -INFINITY;
+        const float gate = stable_sigmoid(lse_nat - sk);
+        m.fac[tid] = gate / l;
+        m.m_used[tid] = -INFINITY;  // the next item starts afresh
+        if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = lse_nat;
+      }
+      named_bar_sync(1, 128);
+      // O^T -> out (bf16) straight from registers once the last PV is done:
+      // for each head, a warp writes 32 consecutive d of that head's row.
+      mbar_wait(smem_u32(&m.o_done), (gb - 1) & 1, fs, 7);
+      tc_fence_after();
+      __nv_bfloat16* out_t = out + (static_cast<size_t>(t) * H + h0) * kDv;
+      for (int j = 0; j < 4; ++j) {
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tmem_ld32_sync(tmem + lane_base + kColO + j * kHG + half * 32, r);
+          const int d = j * 128 + tid;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int h = half * 32 + i;
+            if (h < nh) {
+              const float o = __uint_as_float(r[i]) * m.fac[h];
+              const __nv_bfloat16 hi = __float2bfloat16_rn(o);
+              out_t[static_cast<size_t>(h) * kDv + d] = hi;
+              if (residual)
+                out_t[lo_off + static_cast<size_t>(h) * kDv + d] =
+                    __float2bfloat16_rn(o - __bfloat162float(hi));
+            }
+          }
+        }
+      }
     }
   }
 
@@ -458,8 +488,10 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const in
     attr_done = true;
   }
   const int G = (p.H + kHG - 1) / kHG;
-  const long long grid = static_cast<long long>(p.T) * G;
-  if (grid == 0) return cudaSuccess;
+  const long long items = static_cast<long long>(p.T) * G;
+  if (items == 0) return cudaSuccess;
+  // persistent: at most one CTA per SM, each walking its share of the items
+  const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
   CUtensorMap tm_q, tm_kv;
   const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
   cudaError_t e = make_head_tile_map(&tm_q, q, p.T, p.H, p.d_qk, box_heads);
@@ -467,7 +499,7 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const in
   if (e != cudaSuccess) return e;
   auto kern = p.d_qk == 512 ? fwd_kernel<512> : fwd_kernel<576>;
   const int smem = p.d_qk == 512 ? FwdLayout<512>::kSmemBytes : FwdLayout<576>::kSmemBytes;
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(
+  kern<<<grid, kThreads, smem, s>>>(
       tm_q, tm_kv, idx, len, sink, static_cast<__nv_bfloat16*>(out), lse,
       static_cast<const __nv_bfloat16*>(kv), p.T, p.H, p.S_kv, p.W, p.scale, G,
       p.delta_residual ? 1 : 0, box_heads, p.cu_q, p.cu_kv, p.B);

@@ -34,6 +34,15 @@ struct BwdWorkspace {
                     // contiguous; G = ceil(H / 32), nbmax = ceil(W / 128)
   size_t total;
 };
+// SMs of the current device: the grid size of the persistent kernels.
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 1;
+  return n;
+}
+
 inline int bwd_groups(int H) { return (H + 31) / 32; }
 inline int bwd_nbmax(int W) { return (W + 127) / 128; }
 BwdWorkspace bwd_workspace_layout(const Problem& p);
