@@ -158,23 +158,23 @@ k_bwd_pre(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict
 
 // ------------------------------------------------------------------ b2-b4: dq, dS', P
 
-constexpr int kHG = 32;                  // heads per CTA (UMMA N of S, dP, dQ)
+constexpr int kHG = 64;                  // heads per item (UMMA N of S and dP each, and of dQ)
 constexpr int kThreads = 256;
 constexpr int kProducers = 96;           // warps 5-7
 constexpr int kKVChunk = kBlk * 128;     // 16 KB
-constexpr int kHChunk = kHG * 128;       // 4 KB: 64 columns of 32 head rows
-constexpr int kQdO = 2 * kHChunk;                   // Q chunk x, then dO chunk x
+constexpr int kHChunk = kHG * 128;       // 8 KB: 64 columns of 64 head rows
+constexpr int kStage = 2 * kHChunk;      // Q chunk x (rows 0..63), then dO chunk x (rows 64..127)
+constexpr int kStages = 4;               // ring of (Q, dO) chunk pairs
 
-// TMEM: [S^T | dP^T] (64 columns), then two dQ^T buffers of 5 x 32 columns
-// so that one item's dQ is read out while the next item accumulates.
+// TMEM: [S^T | dP^T] (2 x 64 columns), then dQ^T (5 tiles x 64 columns).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColdP = 32, kColdQ = 64, kDqCols = 160;
+constexpr uint32_t kColS = 0, kColdP = 64, kColdQ = 128;
 
 struct Misc {
   uint64_t kv_full[kChunks];
   uint64_t kv_free[kChunks];
-  uint64_t qd_full, qd_free, s_full, ds_full, rope_done, dsp_free, mma_done;
-  uint64_t dq_full[2], dq_free[2];  // the two dQ^T buffers, by item parity
+  uint64_t qd_full[kStages], qd_free[kStages];
+  uint64_t s_full, ds_full, rope_done, dsp_free, dq_full, mma_done;
   float lse2[kHG], gate[kHG], delta[kHG];
   uint32_t tmem_base;
   int abort_flag;
@@ -186,14 +186,16 @@ struct Misc {
 // of dQ is done), p = 1..8 the V chunks 0..7; blocks are gathered and
 // consumed in the order p = 1..8, 0 because position 0 is released last.
 // Without one, position p holds V chunk p and P has a tile of its own.
+// Q and dO do not stay resident for 64 heads: their chunk x comes in by TMA
+// into a ring stage for each S / dP step.
 template <int kD>
 struct DqLayout {
   static constexpr int kCh = kD / 64;
   static constexpr bool kRope = kCh > 8;
   static constexpr int kDT = (kD + 127) / 128;   // 128-row d tiles of dQ^T
   static constexpr int kOffKV = 0;
-  static constexpr int kOffQD = kOffKV + kCh * kKVChunk;  // 8 (Q, dO) pairs, then Q rope
-  static constexpr int kOffdS = kOffQD + 8 * kQdO + (kRope ? kHChunk : 0);  // 2 sub-tiles
+  static constexpr int kOffQD = kOffKV + kCh * kKVChunk;
+  static constexpr int kOffdS = kOffQD + kStages * kStage;  // 2 sub-tiles of 64 slots
   static constexpr int kOffP = kRope ? kOffKV : kOffdS + 2 * kHChunk;
   static constexpr int kOffMisc = kRope ? kOffdS + 2 * kHChunk : kOffP + 2 * kHChunk;
   static constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
@@ -222,7 +224,7 @@ __device__ __forceinline__ int pos_of_step(int i) {
   return kRope ? (i == kChunks - 1 ? 0 : i + 1) : i;
 }
 
-// Byte offset of element (head row h, slot) in a [32 rows x 128 slots] bf16
+// Byte offset of element (head row h, slot) in a [64 rows x 128 slots] bf16
 // tile kept as two 128B-swizzled sub-tiles of 64 slots: the layout of dS' and
 // P (K-major B for dQ^T; stored to the scratch by TMA, 32 rows x 64 slots
 // per box).
@@ -231,6 +233,12 @@ __device__ __forceinline__ uint32_t hs_tile_off(uint32_t h, uint32_t slot) {
   return (slot >> 6) * kHChunk + h * 128u + ((((col >> 3) ^ (h & 7u)) << 4) | ((col & 7u) << 1));
 }
 
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// Items are (token, 64-head group) pairs; the scratch keeps its rows per
+// 32-head group (G32 groups: dS' rows first, then P rows).
 template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
 k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -239,7 +247,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
          const int32_t* __restrict__ idxc, const int32_t* __restrict__ count,
          const float* __restrict__ lse2_g, const float* __restrict__ gate_g,
          const float* __restrict__ delta_g, __nv_bfloat16* __restrict__ dq, int T, int H, int W,
-         float scale, int G, int box_heads, int nbmax) {
+         float scale, int G, int G32, int box_heads, int nbmax) {
   using L = DqLayout<kD>;
   constexpr int kCh = L::kCh, kDT = L::kDT, kOffKV = L::kOffKV, kOffQD = L::kOffQD,
                 kOffdS = L::kOffdS, kOffP = L::kOffP, kOffMisc = L::kOffMisc;
@@ -254,9 +262,9 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   Misc& m = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const FailState fs{&g_err_bwd, &m.abort_flag};
   // Persistent: CTA c takes items c, c + gridDim.x, ... of the (token, head
-  // group) list.  Every role walks the same items; barrier phases follow a
-  // running count of blocks (per-block barriers) and of non-empty items
-  // (per-item barriers).
+  // group) list.  Every role walks the same items; barrier phases follow
+  // running counts of blocks, of S / dP steps (the Q / dO ring) and of
+  // non-empty items.
   const int n_items = T * G;
 
   if (tid == 0) {
@@ -264,30 +272,31 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       mbar_init(smem_u32(&m.kv_full[c]), kProducers);
       mbar_init(smem_u32(&m.kv_free[c]), 1);
     }
-    mbar_init(smem_u32(&m.qd_full), 1);
-    mbar_init(smem_u32(&m.qd_free), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&m.qd_full[s]), 1);
+      mbar_init(smem_u32(&m.qd_free[s]), 1);
+    }
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.ds_full), 128);
     mbar_init(smem_u32(&m.rope_done), 1);
     mbar_init(smem_u32(&m.dsp_free), 1);
-    for (int u = 0; u < 2; ++u) {
-      mbar_init(smem_u32(&m.dq_full[u]), 1);
-      mbar_init(smem_u32(&m.dq_free[u]), 128);
-    }
+    mbar_init(smem_u32(&m.dq_full), 1);
     mbar_init(smem_u32(&m.mma_done), 1);
     m.abort_flag = 0;
     mbar_init_fence();
   }
-  // Q / dO tile rows the TMA box does not cover (only when H < 32) are zero;
-  // the loads never write them, so once is enough.
-  for (int i = tid; i < (kCh + 8) * (kHG - box_heads) * 8; i += kThreads) {
-    const int per = (kHG - box_heads) * 8;
-    const int c = i / per, rem = i - c * per;
-    const int row = box_heads + rem / 8, pc = rem & 7;
-    const uint32_t base = c < kCh ? sbase + kOffQD + c * kQdO
-                                  : sbase + kOffQD + (c - kCh) * kQdO + kHChunk;
-    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(base + sw128_off(row, pc)), "r"(0u)
-                 : "memory");
+  // Ring rows the TMA boxes do not cover (only when H < 64) are zero; the
+  // loads never write them, so once is enough.
+  {
+    const int per = (kHG - box_heads) * 8;  // 16-byte pieces per half stage
+    for (int i = tid; i < kStages * 2 * per; i += kThreads) {
+      const int half = i / per, rem = i - half * per;  // half = 2 * stage + (0: Q, 1: dO)
+      const int row = (half & 1) * kHG + box_heads + rem / 8, pc = rem & 7;
+      asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(
+                       sbase + kOffQD + (half >> 1) * kStage + sw128_off(row, pc)),
+                   "r"(0u)
+                   : "memory");
+    }
   }
   fence_proxy_async_smem();
   if (warp == 4) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
@@ -299,31 +308,19 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 
   if (warp >= 5) {
     // ------------------------------------------------------------ loads
-    // Per item: the Q and dO tiles of the head group by TMA (once the
-    // previous item's S / dP GEMMs are done with them), then the KV row
-    // gather with cp.async (one warp instruction = 4 whole 128 B row pieces)
-    // into the 128B-swizzled chunk tiles, or by 2-D TMA for a block of
-    // consecutive rows.
+    // Per S / dP step: the (Q, dO) chunk pair of the head group by TMA into
+    // the next ring stage, and the KV chunk of the block: cp.async (one warp
+    // instruction = 4 whole 128 B row pieces) into the 128B-swizzled chunk
+    // tile, or by 2-D TMA for a block of consecutive rows.
     const int pw = warp - 5;
     const uint64_t keep = l2_evict_last();
-    int gb = 0, it = 0;  // blocks and non-empty items so far
+    int gb = 0, gs = 0;  // blocks and steps so far
     for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
       const int t = u / G, h0 = (u - t * G) * kHG;
       const int Kt = count[t];
       if (Kt == 0) continue;
       const int nblk = (Kt + kBlk - 1) / kBlk;
       const int32_t* rows = idxc + static_cast<size_t>(t) * W;
-      if (tid == 160) {
-        if (it > 0) mbar_wait(smem_u32(&m.qd_free), (it - 1) & 1, fs, 11);
-        const uint64_t pol = l2_evict_first();
-        mbar_arrive_expect_tx(smem_u32(&m.qd_full), (kCh + 8) * box_heads * 128);
-        for (int c = 0; c < kCh; ++c)
-          tma_load_3d_hint(sbase + kOffQD + c * kQdO, &tm_q, c * 64, h0, t,
-                           smem_u32(&m.qd_full), pol);
-        for (int c = 0; c < 8; ++c)
-          tma_load_3d_hint(sbase + kOffQD + c * kQdO + kHChunk, &tm_do, c * 64, h0, t,
-                           smem_u32(&m.qd_full), pol);
-      }
       for (int b = 0; b < nblk; ++b, ++gb) {
         // This lane's rows of the block, read once (before the wait on the
         // first chunk, so the reads overlap it) and reused by all chunks.
@@ -350,10 +347,19 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
           for (int i = tid - 160; i < kBlk; i += kProducers) mine &= rows[b * kBlk + i] == r0 + i;
           contig = !named_bar_or(2, kProducers, !mine);
         }
-        for (int i = 0; i < kCh; ++i) {
+        for (int i = 0; i < kCh; ++i, ++gs) {
           const int pos = pos_of_step<kRope>(i);
-          if (gb > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (gb - 1) & 1, fs, 1);
           const int x = dchunk_of_pos<kRope>(pos);
+          if (gb > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (gb - 1) & 1, fs, 1);
+          if (tid == 160) {
+            const int s = gs % kStages, n = gs / kStages;
+            if (n > 0) mbar_wait(smem_u32(&m.qd_free[s]), (n - 1) & 1, fs, 11);
+            const uint32_t st = sbase + kOffQD + s * kStage;
+            mbar_arrive_expect_tx(smem_u32(&m.qd_full[s]), (x < 8 ? 2 : 1) * box_heads * 128);
+            tma_load_3d_hint(st, &tm_q, x * 64, h0, t, smem_u32(&m.qd_full[s]), keep);
+            if (x < 8)
+              tma_load_3d_hint(st + kHChunk, &tm_do, x * 64, h0, t, smem_u32(&m.qd_full[s]), keep);
+          }
           if (contig) {
             if (tid == 160) {
               mbar_arrive_expect_tx(smem_u32(&m.kv_full[pos]), kKVChunk);
@@ -372,7 +378,6 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
           cp_async_arrive(smem_u32(&m.kv_full[pos]));
         }
       }
-      ++it;
     }
     cp_async_wait_all();
   } else if (warp == 4) {
@@ -381,35 +386,35 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       const uint32_t idSdP = idesc_bf16(128, 2 * kHG, false, false);  // [S^T | dP^T]
       const uint32_t idS = idesc_bf16(128, kHG, false, false);         // S^T, rope part
       const uint32_t idQ = idesc_bf16(128, kHG, true, false);  // dQ^T: A MN-major, B K-major
-      int gb = 0, it = 0;
+      int it = 0, gb = 0, gs = 0;
       for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
         const int t = u / G;
         const int Kt = count[t];
         if (Kt == 0) continue;
         const int nblk = (Kt + kBlk - 1) / kBlk;
-        const uint32_t tdq = tmem + kColdQ + (it & 1) * kDqCols;  // this item's dQ^T buffer
-        mbar_wait(smem_u32(&m.qd_full), it & 1, fs, 2);
         for (int b = 0; b < nblk; ++b, ++gb) {
-          for (int i = 0; i < kCh; ++i) {
+          for (int i = 0; i < kCh; ++i, ++gs) {
             const int pos = pos_of_step<kRope>(i);
+            const int x = dchunk_of_pos<kRope>(pos);
+            const int s = gs % kStages, n = gs / kStages;
             mbar_wait(smem_u32(&m.kv_full[pos]), gb & 1, fs, 3);
+            mbar_wait(smem_u32(&m.qd_full[s]), n & 1, fs, 2);
             fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
             tc_fence_after();
-            const int x = dchunk_of_pos<kRope>(pos);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint64_t a = sdesc_sw128(sbase + kOffKV + pos * kKVChunk + k * 32, 16, 1024);
-              // V chunks: S and dP in one N = 64 MMA (B rows: the Q heads, then
-              // the dO heads); the rope chunk adds to S only.
-              const uint64_t bqd = sdesc_sw128(sbase + kOffQD + x * kQdO + k * 32, 16, 1024);
+              // V chunks: S and dP in one N = 128 MMA (B rows: the Q heads,
+              // then the dO heads); the rope chunk adds to S only.
+              const uint64_t bqd = sdesc_sw128(sbase + kOffQD + s * kStage + k * 32, 16, 1024);
               umma_ss(tmem + kColS, a, bqd, x < 8 ? idSdP : idS, (i | k) != 0);
             }
+            umma_commit(smem_u32(&m.qd_free[s]));
           }
           umma_commit(smem_u32(&m.s_full));
-          if (b == nblk - 1) umma_commit(smem_u32(&m.qd_free));  // Q / dO read for the last time
+          // dS' of this block; for the first block of an item this also
+          // orders the softmax warps' read-out of the previous dQ^T first
           mbar_wait(smem_u32(&m.ds_full), gb & 1, fs, 4);
-          // the dQ^T buffer of two items ago has been read out
-          if (b == 0 && it >= 2) mbar_wait(smem_u32(&m.dq_free[it & 1]), ((it >> 1) - 1) & 1, fs, 12);
           tc_fence_after();
           // dQ^T chunks: rope first (its second 64-row atom reads V chunk 0 as
           // filler rows that are never stored), then d rows 0..511.
@@ -422,7 +427,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                   sdesc_sw128(sbase + kOffKV + pos0 * kKVChunk + kk * 2048, kKVChunk, 1024);
               const uint64_t bs =
                   sdesc_sw128(sbase + kOffdS + (kk >> 2) * kHChunk + (kk & 3) * 32, 16, 1024);
-              umma_ss(tdq + j * kHG, a, bs, idQ, (b | kk) != 0);
+              umma_ss(tmem + kColdQ + j * kHG, a, bs, idQ, (b | kk) != 0);
             }
             if (j == 4) {
               umma_commit(smem_u32(&m.rope_done));
@@ -433,7 +438,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
           }
           umma_commit(smem_u32(&m.dsp_free));
         }
-        umma_commit(smem_u32(&m.dq_full[it & 1]));
+        umma_commit(smem_u32(&m.dq_full));
         ++it;
       }
       if (it > 0) {  // all MMAs retired before the TMEM is freed
@@ -445,8 +450,8 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   } else {
     // ------------------------------------------------------------ P, dS', dq
     const float sl2 = scale * kLog2e;
-    const size_t spr = static_cast<size_t>(64) * G;  // scratch rows per (token, block)
-    int gb = 0, it = 0;
+    const size_t spr = static_cast<size_t>(64) * G32;  // scratch rows per (token, block)
+    int it = 0, gb = 0;
     for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
       const int t = u / G, h0 = (u - t * G) * kHG;
       const int nh = min(kHG, H - h0);
@@ -472,27 +477,39 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       for (int b = 0; b < nblk; ++b, ++gb) {
         mbar_wait(smem_u32(&m.s_full), gb & 1, fs, 7);
         tc_fence_after();
-        uint32_t rs[32], rd[32];
-        tmem_ld32x2_sync(tmem + lane_base + kColS, rs, tmem + lane_base + kColdP, rd);
         const bool valid = b * kBlk + tid < Kt;
-        float pv[kHG], dsv[kHG];
+        uint32_t pk[kHG / 2];  // P as bf16 pairs (heads 2i, 2i + 1)
 #pragma unroll
-        for (int h = 0; h < kHG; ++h) {
-          // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
-          const float p =
-              valid ? ex2_approx(fmaf(__uint_as_float(rs[h]), sl2, -m.lse2[h])) * m.gate[h] : 0.f;
-          pv[h] = p;
-          dsv[h] = valid ? p * (__uint_as_float(rd[h]) - m.delta[h]) * scale : 0.f;
-        }
-        if (gb > 0) mbar_wait(smem_u32(&m.dsp_free), (gb - 1) & 1, fs, 8);
-        // thread 0 finished reading the previous block's tiles out (bulk wait below)
-        named_bar_sync(1, 128);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t rs[32], rd[32];
+          tmem_ld32x2_sync(tmem + lane_base + kColS + half * 32, rs,
+                           tmem + lane_base + kColdP + half * 32, rd);
+          float dsv[32];
 #pragma unroll
-        for (int h = 0; h < kHG; ++h) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(dsv[h]);
-          asm volatile("st.shared.b16 [%0], %1;" ::"r"(sbase + kOffdS + hs_tile_off(h, tid)),
-                       "h"(*reinterpret_cast<const unsigned short*>(&v))
-                       : "memory");
+          for (int i = 0; i < 32; i += 2) {
+            float p[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int h = half * 32 + i + e;
+              // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
+              p[e] = valid ? ex2_approx(fmaf(__uint_as_float(rs[i + e]), sl2, -m.lse2[h])) *
+                                 m.gate[h]
+                           : 0.f;
+              dsv[i + e] = valid ? p[e] * (__uint_as_float(rd[i + e]) - m.delta[h]) * scale : 0.f;
+            }
+            pk[half * 16 + i / 2] = pack_bf16x2(p[0], p[1]);
+          }
+          if (half == 0) {
+            if (gb > 0) mbar_wait(smem_u32(&m.dsp_free), (gb - 1) & 1, fs, 8);
+            // thread 0 finished reading the previous block's tiles out (bulk wait below)
+            named_bar_sync(1, 128);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const __nv_bfloat16 v = __float2bfloat16_rn(dsv[i]);
+            st_shared_b16(sbase + kOffdS + hs_tile_off(half * 32 + i, tid),
+                          *reinterpret_cast<const uint16_t*>(&v));
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -501,23 +518,25 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         // has read the rope rows.
         if constexpr (kRope) mbar_wait(smem_u32(&m.rope_done), gb & 1, fs, 9);
 #pragma unroll
-        for (int h = 0; h < kHG; ++h) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(pv[h]);
-          asm volatile("st.shared.b16 [%0], %1;" ::"r"(sbase + kOffP + hs_tile_off(h, tid)),
-                       "h"(*reinterpret_cast<const unsigned short*>(&v))
-                       : "memory");
+        for (int i = 0; i < kHG / 2; ++i) {
+          st_shared_b16(sbase + kOffP + hs_tile_off(2 * i, tid), static_cast<uint16_t>(pk[i]));
+          st_shared_b16(sbase + kOffP + hs_tile_off(2 * i + 1, tid),
+                        static_cast<uint16_t>(pk[i] >> 16));
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (tid == 0) {
-          // dS' and P rows of this head group -> the (token, block) scratch tile
+          // dS' and P rows of this head group -> the (token, block) scratch
+          // tile, in boxes of 32 heads that hold at least one real head
           const int row0 = static_cast<int>((static_cast<size_t>(t) * nbmax + b) * spr) + h0;
           const uint64_t pol = l2_evict_first();
-          for (int half = 0; half < 2; ++half) {
-            tma_store_2d_hint(&tm_sp, half * 64, row0, sbase + kOffdS + half * kHChunk, pol);
-            tma_store_2d_hint(&tm_sp, half * 64, row0 + 32 * G, sbase + kOffP + half * kHChunk,
-                              pol);
-          }
+          for (int half = 0; half < 2; ++half)
+            for (int g2 = 0; g2 * 32 < nh; ++g2) {
+              tma_store_2d_hint(&tm_sp, half * 64, row0 + g2 * 32,
+                                sbase + kOffdS + half * kHChunk + g2 * 4096, pol);
+              tma_store_2d_hint(&tm_sp, half * 64, row0 + 32 * G32 + g2 * 32,
+                                sbase + kOffP + half * kHChunk + g2 * 4096, pol);
+            }
           bulk_commit();
           bulk_wait_read();
           if constexpr (kRope) mbar_arrive(smem_u32(&m.kv_free[0]));  // position 0 may take the next rope rows
@@ -525,22 +544,23 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       }
       // dQ^T -> dq (bf16), straight from registers: for each head, a warp
       // writes 32 consecutive d of that head's row.
-      mbar_wait(smem_u32(&m.dq_full[it & 1]), (it >> 1) & 1, fs, 10);
+      mbar_wait(smem_u32(&m.dq_full), it & 1, fs, 10);
       tc_fence_after();
-      const uint32_t tdq = tmem + lane_base + kColdQ + (it & 1) * kDqCols;
       __nv_bfloat16* dq_t = dq + (static_cast<size_t>(t) * H + h0) * kD;
       for (int j = 0; j < kDT; ++j) {
-        uint32_t v[32];
-        tmem_ld32_sync(tdq + j * kHG, v);
         const int d = j * 128 + tid;
-        if (d < kD) {
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          tmem_ld32_sync(tmem + lane_base + kColdQ + j * kHG + half * 32, v);
+          if (d < kD) {
 #pragma unroll
-          for (int h = 0; h < kHG; ++h)
-            if (h < nh) dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(__uint_as_float(v[h]));
+            for (int i = 0; i < 32; ++i) {
+              const int h = half * 32 + i;
+              if (h < nh) dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(__uint_as_float(v[i]));
+            }
+          }
         }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&m.dq_free[it & 1]));
       ++it;
     }
   }
@@ -888,9 +908,10 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     }
   }
   if ((stages & kBwdMain) && p.T > 0) {
-    const int G = bwd_groups(p.H), nbmax = bwd_nbmax(p.W);
+    const int G32 = bwd_groups(p.H), nbmax = bwd_nbmax(p.W);
+    const int G = (p.H + kHG - 1) / kHG;  // 64-head items
     __nv_bfloat16* sp = reinterpret_cast<__nv_bfloat16*>(base + L.sp);
-    const long long sp_rows = static_cast<long long>(p.T) * nbmax * 64 * G;
+    const long long sp_rows = static_cast<long long>(p.T) * nbmax * 64 * G32;
     CUtensorMap tm_q, tm_do, tm_sp_st, tm_kv;
     const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
     e = make_head_tile_map(&tm_q, q, p.T, p.H, p.d_qk, box_heads);
@@ -906,7 +927,7 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     kern<<<grid, kThreads, smem, s>>>(
         tm_q, tm_do, tm_sp_st, tm_kv, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2,
         gate,
-        delta, static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, box_heads, nbmax);
+        delta, static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, G32, box_heads, nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
