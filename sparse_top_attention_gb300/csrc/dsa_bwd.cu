@@ -159,8 +159,11 @@ k_bwd_pre(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict
 // ------------------------------------------------------------------ b2-b4: dq, dS', P
 
 constexpr int kHG = 64;                  // heads per item (UMMA N of S and dP each, and of dQ)
-constexpr int kThreads = 256;
-constexpr int kProducers = 96;           // warps 5-7
+constexpr int kSoftmax = 256;            // warps 0-7: row (warp & 3) * 32 + lane, heads 32 * (warp >> 2) + 0..31
+constexpr int kMmaWarp = 8;
+constexpr int kIssuer = 288;             // lane 0 of warp 9
+constexpr int kProducers = 96;           // warps 9-11
+constexpr int kThreads = kSoftmax + 32 + kProducers;
 constexpr int kKVChunk = kBlk * 128;     // 16 KB
 constexpr int kHChunk = kHG * 128;       // 8 KB: 64 columns of 64 head rows
 constexpr int kStage = 2 * kHChunk;      // Q chunk x (rows 0..63), then dO chunk x (rows 64..127)
@@ -277,7 +280,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       mbar_init(smem_u32(&m.qd_free[s]), 1);
     }
     mbar_init(smem_u32(&m.s_full), 1);
-    mbar_init(smem_u32(&m.ds_full), 128);
+    mbar_init(smem_u32(&m.ds_full), kSoftmax);
     mbar_init(smem_u32(&m.rope_done), 1);
     mbar_init(smem_u32(&m.dsp_free), 1);
     mbar_init(smem_u32(&m.dq_full), 1);
@@ -299,20 +302,20 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     }
   }
   fence_proxy_async_smem();
-  if (warp == 4) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = m.tmem_base;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
-  if (warp >= 5) {
+  if (warp > kMmaWarp) {
     // ------------------------------------------------------------ loads
     // Per S / dP step: the (Q, dO) chunk pair of the head group by TMA into
     // the next ring stage, and the KV chunk of the block: cp.async (one warp
     // instruction = 4 whole 128 B row pieces) into the 128B-swizzled chunk
     // tile, or by 2-D TMA for a block of consecutive rows.
-    const int pw = warp - 5;
+    const int pw = warp - (kMmaWarp + 1);
     const uint64_t keep = l2_evict_last();
     int gb = 0, gs = 0;  // blocks and steps so far
     for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
@@ -344,14 +347,14 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         if (b * kBlk + kBlk <= Kt) {
           r0 = rows[b * kBlk];
           bool mine = true;
-          for (int i = tid - 160; i < kBlk; i += kProducers) mine &= rows[b * kBlk + i] == r0 + i;
+          for (int i = tid - kIssuer; i < kBlk; i += kProducers) mine &= rows[b * kBlk + i] == r0 + i;
           contig = !named_bar_or(2, kProducers, !mine);
         }
         for (int i = 0; i < kCh; ++i, ++gs) {
           const int pos = pos_of_step<kRope>(i);
           const int x = dchunk_of_pos<kRope>(pos);
           if (gb > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (gb - 1) & 1, fs, 1);
-          if (tid == 160) {
+          if (tid == kIssuer) {
             const int s = gs % kStages, n = gs / kStages;
             if (n > 0) mbar_wait(smem_u32(&m.qd_free[s]), (n - 1) & 1, fs, 11);
             const uint32_t st = sbase + kOffQD + s * kStage;
@@ -361,7 +364,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
               tma_load_3d_hint(st + kHChunk, &tm_do, x * 64, h0, t, smem_u32(&m.qd_full[s]), keep);
           }
           if (contig) {
-            if (tid == 160) {
+            if (tid == kIssuer) {
               mbar_arrive_expect_tx(smem_u32(&m.kv_full[pos]), kKVChunk);
               tma_load_2d_hint(sbase + kOffKV + pos * kKVChunk, &tm_kv, x * 64, r0,
                                smem_u32(&m.kv_full[pos]), keep);
@@ -380,7 +383,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       }
     }
     cp_async_wait_all();
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ UMMA issue
     if (lane == 0) {
       const uint32_t idSdP = idesc_bf16(128, 2 * kHG, false, false);  // [S^T | dP^T]
@@ -449,15 +452,19 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     __syncwarp();
   } else {
     // ------------------------------------------------------------ P, dS', dq
+    // Thread (warp w, lane l) owns gathered row (w & 3) * 32 + l of the
+    // block (its TMEM lane) and heads hb .. hb + 31, hb = 32 * (w >> 2): two
+    // warps per SM sub-partition share the exp2 / FMA work of a block.
     const float sl2 = scale * kLog2e;
     const size_t spr = static_cast<size_t>(64) * G32;  // scratch rows per (token, block)
+    const int row = (warp & 3) * 32 + lane, hb = (warp >> 2) * 32;
     int it = 0, gb = 0;
     for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
       const int t = u / G, h0 = (u - t * G) * kHG;
       const int nh = min(kHG, H - h0);
       const int Kt = count[t];
       if (Kt == 0) {  // empty row: dq = 0, nothing for dkv
-        for (int v = tid; v < nh * (kD / 8); v += 128) {
+        for (int v = tid; v < nh * (kD / 8); v += kSoftmax) {
           const int h = v / (kD / 8), c = v - h * (kD / 8);
           *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kD + c * 8) =
               make_uint4(0, 0, 0, 0);
@@ -473,43 +480,36 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         m.gate[tid] = real ? gate_g[r] : 0.f;
         m.delta[tid] = real ? delta_g[r] : 0.f;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kSoftmax);
       for (int b = 0; b < nblk; ++b, ++gb) {
         mbar_wait(smem_u32(&m.s_full), gb & 1, fs, 7);
         tc_fence_after();
-        const bool valid = b * kBlk + tid < Kt;
-        uint32_t pk[kHG / 2];  // P as bf16 pairs (heads 2i, 2i + 1)
+        const bool valid = b * kBlk + row < Kt;
+        uint32_t rs[32], rd[32];
+        tmem_ld32x2_sync(tmem + lane_base + kColS + hb, rs, tmem + lane_base + kColdP + hb, rd);
+        float dsv[32];
+        uint32_t pk[16];  // P as bf16 pairs (heads hb + 2i, hb + 2i + 1)
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t rs[32], rd[32];
-          tmem_ld32x2_sync(tmem + lane_base + kColS + half * 32, rs,
-                           tmem + lane_base + kColdP + half * 32, rd);
-          float dsv[32];
+        for (int i = 0; i < 32; i += 2) {
+          float p[2];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float p[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int h = half * 32 + i + e;
-              // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
-              p[e] = valid ? ex2_approx(fmaf(__uint_as_float(rs[i + e]), sl2, -m.lse2[h])) *
-                                 m.gate[h]
-                           : 0.f;
-              dsv[i + e] = valid ? p[e] * (__uint_as_float(rd[i + e]) - m.delta[h]) * scale : 0.f;
-            }
-            pk[half * 16 + i / 2] = pack_bf16x2(p[0], p[1]);
+          for (int e = 0; e < 2; ++e) {
+            const int h = hb + i + e;
+            // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
+            p[e] = valid ? ex2_approx(fmaf(__uint_as_float(rs[i + e]), sl2, -m.lse2[h])) * m.gate[h]
+                         : 0.f;
+            dsv[i + e] = valid ? p[e] * (__uint_as_float(rd[i + e]) - m.delta[h]) * scale : 0.f;
           }
-          if (half == 0) {
-            if (gb > 0) mbar_wait(smem_u32(&m.dsp_free), (gb - 1) & 1, fs, 8);
-            // thread 0 finished reading the previous block's tiles out (bulk wait below)
-            named_bar_sync(1, 128);
-          }
+          pk[i / 2] = pack_bf16x2(p[0], p[1]);
+        }
+        if (gb > 0) mbar_wait(smem_u32(&m.dsp_free), (gb - 1) & 1, fs, 8);
+        // thread 0 finished reading the previous block's tiles out (bulk wait below)
+        named_bar_sync(1, kSoftmax);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const __nv_bfloat16 v = __float2bfloat16_rn(dsv[i]);
-            st_shared_b16(sbase + kOffdS + hs_tile_off(half * 32 + i, tid),
-                          *reinterpret_cast<const uint16_t*>(&v));
-          }
+        for (int i = 0; i < 32; ++i) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(dsv[i]);
+          st_shared_b16(sbase + kOffdS + hs_tile_off(hb + i, row),
+                        *reinterpret_cast<const uint16_t*>(&v));
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -518,13 +518,13 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         // has read the rope rows.
         if constexpr (kRope) mbar_wait(smem_u32(&m.rope_done), gb & 1, fs, 9);
 #pragma unroll
-        for (int i = 0; i < kHG / 2; ++i) {
-          st_shared_b16(sbase + kOffP + hs_tile_off(2 * i, tid), static_cast<uint16_t>(pk[i]));
-          st_shared_b16(sbase + kOffP + hs_tile_off(2 * i + 1, tid),
+        for (int i = 0; i < 16; ++i) {
+          st_shared_b16(sbase + kOffP + hs_tile_off(hb + 2 * i, row), static_cast<uint16_t>(pk[i]));
+          st_shared_b16(sbase + kOffP + hs_tile_off(hb + 2 * i + 1, row),
                         static_cast<uint16_t>(pk[i] >> 16));
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kSoftmax);
         if (tid == 0) {
           // dS' and P rows of this head group -> the (token, block) scratch
           // tile, in boxes of 32 heads that hold at least one real head
@@ -548,16 +548,14 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       tc_fence_after();
       __nv_bfloat16* dq_t = dq + (static_cast<size_t>(t) * H + h0) * kD;
       for (int j = 0; j < kDT; ++j) {
-        const int d = j * 128 + tid;
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32];
-          tmem_ld32_sync(tmem + lane_base + kColdQ + j * kHG + half * 32, v);
-          if (d < kD) {
+        const int d = j * 128 + row;
+        uint32_t v[32];
+        tmem_ld32_sync(tmem + lane_base + kColdQ + j * kHG + hb, v);
+        if (d < kD) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int h = half * 32 + i;
-              if (h < nh) dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(__uint_as_float(v[i]));
-            }
+          for (int i = 0; i < 32; ++i) {
+            const int h = hb + i;
+            if (h < nh) dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(__uint_as_float(v[i]));
           }
         }
       }
@@ -568,7 +566,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------ b5-b6: dKV
