@@ -21,15 +21,18 @@
 //     boundary failures", Summary 1-3: empty rows, padded columns masked to
 //     -inf, a sink that stays finite when it saturates.
 //
-// Warp roles (256 threads):
-//   warps 0-3  softmax and epilogue; thread i owns TMEM lane i (gathered row i)
-//   warp 4     TMEM allocation and the single UMMA-issuing thread
-//   warps 5-7  lane 0 of warp 5 issues the Q tile TMA (3-D tensor map) at
-//              kernel entry; the three warps gather KV rows with cp.async into
-//              128B-swizzled shared tiles, or a whole block of consecutive
-//              rows (the sliding window) with 2-D TMA
-// Eight warps keep two warps per SM sub-partition, so each thread may use up
-// to 255 registers.
+// Warp roles (384 threads):
+//   warps 0-7  softmax and epilogue; thread (w, l) owns TMEM lane
+//              32 (w % 4) + l (gathered row) and heads 32 (w / 4) .. +31, so
+//              two softmax warps share each SM sub-partition's exp2 work
+//   warp 8     TMEM allocation and the single UMMA-issuing thread
+//   warps 9-11 per item: compact the token's index row, lane 0 of warp 9
+//              loads the Q tile by TMA (3-D tensor map), then the three warps
+//              gather KV rows with cp.async into 128B-swizzled shared tiles,
+//              or a whole block of consecutive rows (the sliding window) with
+//              2-D TMA
+// The kernel is persistent: one CTA per SM walks the (token, head group)
+// items, so an item's epilogue overlaps the next item's first gather.
 #include <cmath>
 
 #include "dsa_common.cuh"
@@ -42,9 +45,11 @@ namespace {
 __device__ unsigned int g_err_fwd;
 
 constexpr int kHG = 64;                      // heads per CTA (UMMA N)
-constexpr int kThreads = 256;
-constexpr int kQIssuer = 160;               // lane 0 of warp 5
-constexpr int kProducers = 96;              // warps 5-7
+constexpr int kSoftmax = 256;               // warps 0-7: row (warp & 3) * 32 + lane, heads 32 * (warp >> 2) + 0..31
+constexpr int kMmaWarp = 8;
+constexpr int kQIssuer = 288;               // lane 0 of warp 9
+constexpr int kProducers = 96;              // warps 9-11
+constexpr int kThreads = kSoftmax + 32 + kProducers;
 constexpr int kQChunk = kHG * 128;           // one 64-column chunk of Q: 8 KB
 constexpr int kKVChunk = kBlk * 128;         // one 64-column chunk of 128 rows: 16 KB
 constexpr int kIdxRegs = (kMaxW + kProducers - 1) / kProducers;  // index row per producer
@@ -137,7 +142,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     mbar_init(smem_u32(&m.q_full), 1);
     mbar_init(smem_u32(&m.q_free), 1);
     mbar_init(smem_u32(&m.s_full), 1);
-    mbar_init(smem_u32(&m.p_full), 128);
+    mbar_init(smem_u32(&m.p_full), kSoftmax);
     mbar_init(smem_u32(&m.o_done), 1);
     mbar_init(smem_u32(&m.mma_done), 1);
     m.abort_flag = 0;
@@ -156,13 +161,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                  : "memory");
   }
   fence_proxy_async_smem();
-  if (warp == 4) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = m.tmem_base;
 
-  if (warp >= 5) {
+  if (warp > kMmaWarp) {
     // ------------------------------------------------------------ gather
     // Per item: compact the token's valid slots into the row list (slot
     // order), load the Q tile of the head group by TMA once the previous
@@ -171,7 +176,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     // instruction moves 4 whole 128-byte row pieces; rows past the valid
     // count are zero-filled and their scores masked), or one 2-D TMA load
     // per chunk for a block of consecutive rows (the sliding window).
-    const int ptid = tid - kQIssuer, pw = warp - 5;
+    const int ptid = tid - kQIssuer, pw = warp - (kMmaWarp + 1);
     const uint64_t keep = l2_evict_last();
     int it = 0, gb = 0;  // non-empty items and blocks so far
     for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
@@ -240,7 +245,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       ++it;
     }
     cp_async_wait_all();
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ UMMA issue
     const uint32_t idS = idesc_bf16(128, kHG, false, false);
     const uint32_t idPV = idesc_bf16(128, kHG, true, true);
@@ -298,9 +303,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    // Thread (warp w, lane l) owns gathered row (w & 3) * 32 + l of the
+    // block (its TMEM lane) and heads hb .. hb + 31, hb = 32 * (w >> 2): two
+    // warps per SM sub-partition share the exp2 work of a block.
     const float sl2 = scale * kLog2e;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS_row = tmem + lane_base + kColS;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int row = (warp & 3) * 32 + lane, hb = (warp >> 2) * 32;
     int gb = 0;
     for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
       const int t = u / G, h0 = (u - t * G) * kHG;
@@ -309,7 +317,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
                                       slot_len(topk_length, t, W),
                                       kv_range(cu_q, cu_kv, B, t, S_kv), lane);
       if (Kt == 0) {  // empty row: out = 0, lse = -FLT_MAX, no tensor-core work
-        for (int v = tid; v < nh * (kDv / 8); v += 128) {
+        for (int v = tid; v < nh * (kDv / 8); v += kSoftmax) {
           const int h = v / (kDv / 8), c = v - h * (kDv / 8);
           const size_t o = (static_cast<size_t>(t) * H + h0 + h) * kDv + c * 8;
           *reinterpret_cast<uint4*>(out + o) = make_uint4(0, 0, 0, 0);
@@ -319,23 +327,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         continue;
       }
       const int nblk = (Kt + kBlk - 1) / kBlk;
-      float lp[kHG];
+      float lp[32];
 #pragma unroll
-      for (int h = 0; h < kHG; ++h) lp[h] = 0.f;
+      for (int h = 0; h < 32; ++h) lp[h] = 0.f;
 
       for (int b = 0; b < nblk; ++b) {
         const int g = gb + b;
         mbar_wait(smem_u32(&m.s_full), g & 1, fs, 5);
         tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld32x2_sync(tS_row, r0, tS_row + 32, r1);
-        const bool valid = b * kBlk + tid < Kt;
-        float s[kHG];
+        uint32_t r0[32];
+        tmem_ld32_sync(tmem + lane_base + kColS + hb, r0);
+        const bool valid = b * kBlk + row < Kt;
+        float s[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = valid ? __uint_as_float(r0[i]) * sl2 : -INFINITY;
-          s[32 + i] = valid ? __uint_as_float(r1[i]) * sl2 : -INFINITY;
-        }
+        for (int i = 0; i < 32; ++i) s[i] = valid ? __uint_as_float(r0[i]) * sl2 : -INFINITY;
         // Lazy rescale: a head keeps its shift unless the block's maximum
         // exceeds it by more than 2^8; the final normalisation uses the same
         // shift for O and l.  The column maxima are only needed when some
@@ -343,17 +348,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         // block), so one vote decides whether to compute them.
         bool above = false;
 #pragma unroll
-        for (int h = 0; h < kHG; ++h) above |= s[h] > m.m_used[h] + 8.f;
-        bool any = named_bar_or(1, 128, above);
+        for (int i = 0; i < 32; ++i) above |= s[i] > m.m_used[hb + i] + 8.f;
+        bool any = named_bar_or(1, kSoftmax, above);
         if (any) {
           // column (per-head) maximum over the 128 gathered rows
-          float* red = m.red[g & 1][warp];
+          float* red = m.red[g & 1][warp & 3];
 #pragma unroll
-          for (int h = 0; h < kHG; ++h) {
-            const float mx = warp_max(s[h]);
-            if ((h & 31) == lane) red[h] = mx;
+          for (int i = 0; i < 32; ++i) {
+            const float mx = warp_max(s[i]);
+            if (i == lane) red[hb + i] = mx;
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(1, kSoftmax);
           bool resc = false;
           if (tid < kHG) {
             const float bm = fmaxf(fmaxf(m.red[g & 1][0][tid], m.red[g & 1][1][tid]),
@@ -364,43 +369,45 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             m.fac[tid] = resc ? ex2_approx(mo - mn) : 1.f;
             if (resc) m.m_used[tid] = mn;
           }
-          any = named_bar_or(1, 128, resc);
+          any = named_bar_or(1, kSoftmax, resc);
         }
         if (any) {
 #pragma unroll
-          for (int h = 0; h < kHG; ++h) lp[h] *= m.fac[h];
+          for (int i = 0; i < 32; ++i) lp[i] *= m.fac[hb + i];
+        }
+        if (any && b > 0) {
+          // O^T columns of heads whose shift moved: scale by 2^(old - new).
+          // The previous PV finished before this block's S (in-order
+          // completion), so the wait returns at once.
+          mbar_wait(smem_u32(&m.o_done), (g - 1) & 1, fs, 6);
+          tc_fence_after();
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t ta = tmem + lane_base + kColO + j * kHG + hb;
+            uint32_t r[32];
+            tmem_ld32_sync(ta, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              r[i] = __float_as_uint(__uint_as_float(r[i]) * m.fac[hb + i]);
+            tmem_st32(ta, r);
+          }
+          tmem_wait_st();
         }
         // P^T row as bf16 pairs; s[] is dead after this loop.
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(s[2 * i] - m.m_used[2 * i]);
-          const float p1 = ex2_approx(s[2 * i + 1] - m.m_used[2 * i + 1]);
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(s[2 * i] - m.m_used[hb + 2 * i]);
+          const float p1 = ex2_approx(s[2 * i + 1] - m.m_used[hb + 2 * i + 1]);
           lp[2 * i] += p0;
           lp[2 * i + 1] += p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
-        if (any && b > 0) {
-          // O^T columns of heads whose shift moved: scale by 2^(old - new).
-          mbar_wait(smem_u32(&m.o_done), (g - 1) & 1, fs, 6);
-          tc_fence_after();
-          for (int j = 0; j < 4; ++j) {
-            for (int half = 0; half < 2; ++half) {
-              const uint32_t ta = tmem + lane_base + kColO + j * kHG + half * 32;
-              uint32_t r[32];
-              tmem_ld32_sync(ta, r);
+        // Store into the swizzled MN-major tile that the PV UMMA reads: this
+        // thread's heads are 16-byte pieces hb / 8 .. hb / 8 + 3 of its row.
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                r[i] = __float_as_uint(__uint_as_float(r[i]) * m.fac[half * 32 + i]);
-              tmem_st32(ta, r);
-            }
-          }
-          tmem_wait_st();
-        }
-        // Store into the swizzled MN-major tile that the PV UMMA reads.
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t dst = sbase + kOffP + sw128_off(tid, c);
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t dst = sbase + kOffP + sw128_off(row, hb / 8 + c);
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(pk[4 * c]),
                        "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                        : "memory");
@@ -413,21 +420,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 
       // ---------------------------------------------------------- epilogue
       // l per head: a butterfly reduce-scatter leaves lane L of each warp
-      // with its warp's sums for heads 2L and 2L + 1 in lp[0..1]; the four
-      // warps' partials meet in shared memory (both halves of red are free:
-      // the block loop's last barrier came after their last reads).
+      // with its rows' sum for head hb + L in lp[0]; the four row warps'
+      // partials meet in shared memory (both halves of red are free: the
+      // block loop's last barrier came after their last reads).
 #pragma unroll
-      for (int o = 16, n = 32; o > 0; o >>= 1, n >>= 1) {
+      for (int o = 16; o > 0; o >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
-        for (int i = 0; i < n; ++i) {
-          const float keep = up ? lp[i + n] : lp[i];
-          const float send = up ? lp[i] : lp[i + n];
+        for (int i = 0; i < o; ++i) {
+          const float keep = up ? lp[i + o] : lp[i];
+          const float send = up ? lp[i] : lp[i + o];
           lp[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
       }
-      *reinterpret_cast<float2*>(&m.red[0][warp][2 * lane]) = make_float2(lp[0], lp[1]);
-      named_bar_sync(1, 128);
+      m.red[0][warp & 3][hb + lane] = lp[0];
+      named_bar_sync(1, kSoftmax);
       if (tid < kHG) {
         const float l = (m.red[0][0][tid] + m.red[0][1][tid]) + (m.red[0][2][tid] + m.red[0][3][tid]);
         const float lse_nat = (m.m_used[tid] + log2f(l)) * kLn2;
@@ -437,28 +444,26 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         m.m_used[tid] = -INFINITY;  // the next item starts afresh
         if (tid < nh) lse[static_cast<size_t>(t) * H + h0 + tid] = lse_nat;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kSoftmax);
       // O^T -> out (bf16) straight from registers once the last PV is done:
       // for each head, a warp writes 32 consecutive d of that head's row.
       mbar_wait(smem_u32(&m.o_done), (gb - 1) & 1, fs, 7);
       tc_fence_after();
       __nv_bfloat16* out_t = out + (static_cast<size_t>(t) * H + h0) * kDv;
       for (int j = 0; j < 4; ++j) {
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tmem_ld32_sync(tmem + lane_base + kColO + j * kHG + half * 32, r);
-          const int d = j * 128 + tid;
+        uint32_t r[32];
+        tmem_ld32_sync(tmem + lane_base + kColO + j * kHG + hb, r);
+        const int d = j * 128 + row;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int h = half * 32 + i;
-            if (h < nh) {
-              const float o = __uint_as_float(r[i]) * m.fac[h];
-              const __nv_bfloat16 hi = __float2bfloat16_rn(o);
-              out_t[static_cast<size_t>(h) * kDv + d] = hi;
-              if (residual)
-                out_t[lo_off + static_cast<size_t>(h) * kDv + d] =
-                    __float2bfloat16_rn(o - __bfloat162float(hi));
-            }
+        for (int i = 0; i < 32; ++i) {
+          const int h = hb + i;
+          if (h < nh) {
+            const float o = __uint_as_float(r[i]) * m.fac[h];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(o);
+            out_t[static_cast<size_t>(h) * kDv + d] = hi;
+            if (residual)
+              out_t[lo_off + static_cast<size_t>(h) * kDv + d] =
+                  __float2bfloat16_rn(o - __bfloat162float(hi));
           }
         }
       }
@@ -468,7 +473,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
