@@ -178,7 +178,9 @@ struct Misc {
   uint64_t kv_free[kChunks];
   uint64_t qd_full[kStages], qd_free[kStages];
   uint64_t s_full, ds_full, rope_done, dsp_free, dq_full, mma_done;
-  float lse2[kHG], gate[kHG], delta[kHG];
+  // per head of the item: (log2(gate) - lse * log2(e), delta), so that
+  // P = exp2(s * scale * log2(e) + x) and one 16-byte load serves two heads
+  alignas(16) float2 cd[kHG];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -476,9 +478,9 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         // Padded heads get gate 0, hence P = dS = 0: they add nothing anywhere.
         const bool real = tid < nh;
         const size_t r = static_cast<size_t>(t) * H + h0 + tid;
-        m.lse2[tid] = real ? lse2_g[r] : 0.f;
-        m.gate[tid] = real ? gate_g[r] : 0.f;
-        m.delta[tid] = real ? delta_g[r] : 0.f;
+        const float gt = real ? gate_g[r] : 0.f;
+        m.cd[tid] = make_float2(gt > 0.f ? log2f(gt) - lse2_g[r] : -INFINITY,
+                                real ? delta_g[r] : 0.f);
       }
       named_bar_sync(1, kSoftmax);
       for (int b = 0; b < nblk; ++b, ++gb) {
@@ -489,18 +491,17 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         tmem_ld32x2_sync(tmem + lane_base + kColS + hb, rs, tmem + lane_base + kColdP + hb, rd);
         float dsv[32];
         uint32_t pk[16];  // P as bf16 pairs (heads hb + 2i, hb + 2i + 1)
+        const float4* cd4 = reinterpret_cast<const float4*>(m.cd + hb);
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          float p[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int h = hb + i + e;
-            // Live columns satisfy s - lse <= 0, so exp2 never overflows here.
-            p[e] = valid ? ex2_approx(fmaf(__uint_as_float(rs[i + e]), sl2, -m.lse2[h])) * m.gate[h]
-                         : 0.f;
-            dsv[i + e] = valid ? p[e] * (__uint_as_float(rd[i + e]) - m.delta[h]) * scale : 0.f;
-          }
-          pk[i / 2] = pack_bf16x2(p[0], p[1]);
+          const float4 c = cd4[i / 2];  // heads hb + i, hb + i + 1
+          // Live columns satisfy s - lse <= 0, so exp2 never overflows here;
+          // rows past the valid count hold zero KV (finite dP) and get P = 0.
+          const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(rs[i]), sl2, c.x)) : 0.f;
+          const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(rs[i + 1]), sl2, c.z)) : 0.f;
+          dsv[i] = p0 * (__uint_as_float(rd[i]) - c.y) * scale;
+          dsv[i + 1] = p1 * (__uint_as_float(rd[i + 1]) - c.w) * scale;
+          pk[i / 2] = pack_bf16x2(p0, p1);
         }
         if (gb > 0) mbar_wait(smem_u32(&m.dsp_free), (gb - 1) & 1, fs, 8);
         // thread 0 finished reading the previous block's tiles out (bulk wait below)

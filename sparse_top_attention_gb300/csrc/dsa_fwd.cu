@@ -64,7 +64,7 @@ struct Misc {
   uint64_t kv_free[kChunks];
   uint64_t q_full, q_free, s_full, p_full, o_done, mma_done;
   float red[2][4][kHG];   // per-warp column maxima, double-buffered by block parity
-  float m_used[kHG];      // running shift per head (log2 units)
+  alignas(16) float m_used[kHG];  // running shift per head (log2 units)
   float fac[kHG];         // rescale factor per head, then the output scale
   int warp_counts[kThreads / 32];
   uint32_t tmem_base;
@@ -347,8 +347,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         // score is that far above its head's shift (always in the first
         // block), so one vote decides whether to compute them.
         bool above = false;
+        const float4* mu4 = reinterpret_cast<const float4*>(m.m_used + hb);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) above |= s[i] > m.m_used[hb + i] + 8.f;
+        for (int i = 0; i < 32; i += 4) {
+          const float4 mu = mu4[i / 4];
+          above |= (s[i] > mu.x + 8.f) | (s[i + 1] > mu.y + 8.f) | (s[i + 2] > mu.z + 8.f) |
+                   (s[i + 3] > mu.w + 8.f);
+        }
         bool any = named_bar_or(1, kSoftmax, above);
         if (any) {
           // column (per-head) maximum over the 128 gathered rows
@@ -396,12 +401,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         // P^T row as bf16 pairs; s[] is dead after this loop.
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(s[2 * i] - m.m_used[hb + 2 * i]);
-          const float p1 = ex2_approx(s[2 * i + 1] - m.m_used[hb + 2 * i + 1]);
+        for (int i = 0; i < 16; i += 2) {
+          const float4 mu = mu4[i / 2];
+          const float p0 = ex2_approx(s[2 * i] - mu.x);
+          const float p1 = ex2_approx(s[2 * i + 1] - mu.y);
+          const float p2 = ex2_approx(s[2 * i + 2] - mu.z);
+          const float p3 = ex2_approx(s[2 * i + 3] - mu.w);
           lp[2 * i] += p0;
           lp[2 * i + 1] += p1;
+          lp[2 * i + 2] += p2;
+          lp[2 * i + 3] += p3;
           pk[i] = pack_bf16x2(p0, p1);
+          pk[i + 1] = pack_bf16x2(p2, p3);
         }
         // Store into the swizzled MN-major tile that the PV UMMA reads: this
         // thread's heads are 16-byte pieces hb / 8 .. hb / 8 + 3 of its row.
