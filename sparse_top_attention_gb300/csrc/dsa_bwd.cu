@@ -5,9 +5,10 @@
 //   k_compact   a1: valid KV rows of every token, in slot order, and counts
 //   k_bwd_pre   b1: delta = rowsum(dout * out), lse*log2(e), gate and the
 //               per-(t,h) d_sink terms (FlashAttention "dpsum" preprocess)
-//   k_bwd_dq    b2-b5: per (token, 32-head group) recompute P, form dS,
+//   k_bwd_dq    b2-b5: per (token, 64-head group) recompute P, form dS,
 //               accumulate dQ in TMEM and store dq; write the dS' and P
-//               tiles of every 128-slot block to a bf16 scratch
+//               tiles of every 128-slot block to a bf16 scratch.  One
+//               persistent CTA per SM walks the (token, group) items.
 //   k_bwd_dkv   b6: per token, dKV_blk^T = [Q^T | dO^T] [dS'; P] over all
 //               heads at once, scatter-added into the fp32 accumulator
 //   k_dkv_cast  fp32 accumulator -> bf16 dkv (k_dkv_cast_fixed for the int64
@@ -37,12 +38,15 @@
 // Rows are D = 576 columns (512 V + 64 rope) or 512 (no rope part); the
 // kernels are templates over D.
 // k_bwd_dq tiles, transposed like the forward: gathered rows are UMMA M
-// (128) and the 32 heads of the group are N.
-//   [S^T | dP^T] = KV_blk . [Q^T | dO^T]  M=128 N=64  K=512, then S^T += rope part (N=32, K=64)
-//   dQ^T += KV_blk^T . dS'^T             ceil(D/128) x (M=128 N=32 K=128)
+// (128) and the 64 heads of the group are N.
+//   [S^T | dP^T] = KV_blk . [Q^T | dO^T]  M=128 N=128 K=512, then S^T += rope part (N=64, K=64)
+//   dQ^T += KV_blk^T . dS'^T             ceil(D/128) x (M=128 N=64 K=128)
 // where dS' = scale * dS.  dS'^T and P^T tiles are written to the scratch.
 // A block of 128 consecutive KV rows (the sliding window) is loaded by 2-D
-// TMA; other blocks row by row with cp.async.
+// TMA; other blocks row by row with cp.async.  Q and dO of 64 heads do not
+// fit beside a 128-row KV block, so each S / dP step brings its 64-column
+// (Q, dO) chunk pair in by TMA through a 4-stage ring.  Two softmax
+// warpgroups split the 64 heads of each gathered row.
 // k_bwd_dkv tiles, per 128-slot block of one token, d rows on the M side:
 //   dKV_blk^T[d, slots] = [Q^T | dO^T][d, 2 x 32G] . [dS'; P][2 x 32G, slots]
 // (dO^T is zero for the 64 rope rows), so the dKV GEMM sees all heads at once
