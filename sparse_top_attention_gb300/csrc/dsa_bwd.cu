@@ -167,7 +167,8 @@ constexpr int kSoftmax = 256;            // warps 0-7: row (warp & 3) * 32 + lan
 constexpr int kMmaWarp = 8;
 constexpr int kIssuer = 288;             // lane 0 of warp 9
 constexpr int kProducers = 96;           // warps 9-11
-constexpr int kThreads = kSoftmax + 32 + kProducers;
+constexpr int kLoaderWarp = 12;          // lane 0 streams the (Q, dO) chunk pairs
+constexpr int kThreads = kSoftmax + 32 + kProducers + 32;
 constexpr int kKVChunk = kBlk * 128;     // 16 KB
 constexpr int kHChunk = kHG * 128;       // 8 KB: 64 columns of 64 head rows
 constexpr int kStage = 2 * kHChunk;      // Q chunk x (rows 0..63), then dO chunk x (rows 64..127)
@@ -315,17 +316,42 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   const uint32_t tmem = m.tmem_base;
   const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
-  if (warp > kMmaWarp) {
-    // ------------------------------------------------------------ loads
-    // Per S / dP step: the (Q, dO) chunk pair of the head group by TMA into
-    // the next ring stage, and the KV chunk of the block: cp.async (one warp
-    // instruction = 4 whole 128 B row pieces) into the 128B-swizzled chunk
-    // tile, or by 2-D TMA for a block of consecutive rows.
+  if (warp == kLoaderWarp) {
+    // ------------------------------------------------------------ Q / dO ring
+    // The (Q, dO) chunk pair of every S / dP step by TMA, each as soon as its
+    // ring stage is free: the first stages of a block fill while the softmax
+    // and dQ of the previous block run.
+    if (lane == 0) {
+      const uint64_t keep = l2_evict_last();
+      int gs = 0;
+      for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
+        const int t = u / G, h0 = (u - t * G) * kHG;
+        const int Kt = count[t];
+        if (Kt == 0) continue;
+        const int nsteps = (Kt + kBlk - 1) / kBlk * kCh;
+        for (int k = 0; k < nsteps; ++k, ++gs) {
+          const int x = dchunk_of_pos<kRope>(pos_of_step<kRope>(k % kCh));
+          const int s = gs % kStages, n = gs / kStages;
+          if (n > 0) mbar_wait(smem_u32(&m.qd_free[s]), (n - 1) & 1, fs, 11);
+          const uint32_t st = sbase + kOffQD + s * kStage;
+          mbar_arrive_expect_tx(smem_u32(&m.qd_full[s]), (x < 8 ? 2 : 1) * box_heads * 128);
+          tma_load_3d_hint(st, &tm_q, x * 64, h0, t, smem_u32(&m.qd_full[s]), keep);
+          if (x < 8)
+            tma_load_3d_hint(st + kHChunk, &tm_do, x * 64, h0, t, smem_u32(&m.qd_full[s]), keep);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp > kMmaWarp) {
+    // ------------------------------------------------------------ KV gather
+    // The KV chunk of each S / dP step: cp.async (one warp instruction = 4
+    // whole 128 B row pieces) into the 128B-swizzled chunk tile, or by 2-D
+    // TMA for a block of consecutive rows.
     const int pw = warp - (kMmaWarp + 1);
     const uint64_t keep = l2_evict_last();
-    int gb = 0, gs = 0;  // blocks and steps so far
+    int gb = 0;  // blocks so far
     for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
-      const int t = u / G, h0 = (u - t * G) * kHG;
+      const int t = u / G;
       const int Kt = count[t];
       if (Kt == 0) continue;
       const int nblk = (Kt + kBlk - 1) / kBlk;
@@ -356,19 +382,10 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
           for (int i = tid - kIssuer; i < kBlk; i += kProducers) mine &= rows[b * kBlk + i] == r0 + i;
           contig = !named_bar_or(2, kProducers, !mine);
         }
-        for (int i = 0; i < kCh; ++i, ++gs) {
+        for (int i = 0; i < kCh; ++i) {
           const int pos = pos_of_step<kRope>(i);
           const int x = dchunk_of_pos<kRope>(pos);
           if (gb > 0) mbar_wait(smem_u32(&m.kv_free[pos]), (gb - 1) & 1, fs, 1);
-          if (tid == kIssuer) {
-            const int s = gs % kStages, n = gs / kStages;
-            if (n > 0) mbar_wait(smem_u32(&m.qd_free[s]), (n - 1) & 1, fs, 11);
-            const uint32_t st = sbase + kOffQD + s * kStage;
-            mbar_arrive_expect_tx(smem_u32(&m.qd_full[s]), (x < 8 ? 2 : 1) * box_heads * 128);
-            tma_load_3d_hint(st, &tm_q, x * 64, h0, t, smem_u32(&m.qd_full[s]), keep);
-            if (x < 8)
-              tma_load_3d_hint(st + kHChunk, &tm_do, x * 64, h0, t, smem_u32(&m.qd_full[s]), keep);
-          }
           if (contig) {
             if (tid == kIssuer) {
               mbar_arrive_expect_tx(smem_u32(&m.kv_full[pos]), kKVChunk);
