@@ -1,8 +1,9 @@
 // Sparse MLA (DSA) forward for sm_103a.
 //
-// One CTA computes one token t for a group of up to 64 query heads.  The
-// token's top-k rows are gathered from the shared KV tensor, 128 rows at a
-// time ("blocks").  The contractions use 5th-gen tensor cores with fp32
+// A work item is one token t with a group of up to 64 query heads; each
+// persistent CTA processes a share of the items in turn.  The token's top-k
+// rows are gathered from the shared KV tensor, 128 rows at a time
+// ("blocks").  The contractions use 5th-gen tensor cores with fp32
 // accumulators in TMEM, in a transposed orientation: the gathered rows form
 // the UMMA M dimension (128) and the heads form N (64), so a 64-head group
 // fills a full-rate M=128 tile.
@@ -10,7 +11,7 @@
 //   O^T[d, h]    += sum_slot V[slot, d] * P^T[slot, h]   (4 x M=128, N=64, K=128)
 // with rows of D = 576 columns (512 V + 64 rope) or 512 (a template
 // parameter).  The softmax runs on S^T in registers, one thread per gathered
-// row, with a lazy rescale: a head's shift only moves when a score exceeds it
+// row and 32 heads, with a lazy rescale: a head's shift only moves when a score exceeds it
 // by more than 2^8.  The sink enters at the end, as sigma(lse - sink):
 //   out = O * sigma(lse - sink) / l.
 // Sources:
