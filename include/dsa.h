@@ -164,7 +164,7 @@ dsa_status_t dsa_bwd(const dsa_problem_t* problem, const void* q, const void* kv
  * and with one workspace; together they equal one dsa_bwd call.
  *   dsa_bwd_preprocess  memset of the dkv accumulator, slot compaction and
  *                       the delta preprocess
- *   dsa_bwd_main        P recompute, dS and dq for every 32-head group, which
+ *   dsa_bwd_main        P recompute, dS and dq for every 64-head group, which
  *                       also stores the dS' and P tiles into the workspace
  *   dsa_bwd_finalize    the dkv tile GEMM over all heads with its
  *                       scatter-add, the dkv fp32 -> bf16 cast and the
