@@ -643,15 +643,15 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
   constexpr int kNT = (kD + 127) / 128;  // 128-row d tiles (the last may be a 64-row rope tile)
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t = blockIdx.x;
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {
     if (tid == 0) atomicCAS(&g_err_bwd, 0u, 0x3FFu);
     return;
   }
-  const int Kt = count[t];
-  if (Kt == 0) return;
-  const int nblk = (Kt + kBlk - 1) / kBlk;
+  // CTA c takes tokens c, c + gridDim.x, ... (one token each when the grid
+  // is T); barrier phases follow running counts of blocks and of (block,
+  // d tile) units, so with fewer CTAs the TMA warp loads the next token's
+  // tiles while the drain finishes this one.
   dkv::Misc& m = *reinterpret_cast<dkv::Misc*>(smem + dkv::kOffMisc);
   const FailState fs{&g_err_bwd, &m.abort_flag};
   const int HP = 32 * G;                          // padded head rows per half
@@ -695,26 +695,33 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
 
   if (warp == kTmaWarp) {
     if (lane == 0) {
-      for (int b = 0; b < nblk; ++b) {
-        if (b > 0) mbar_wait(smem_u32(&m.b_empty), (b - 1) & 1, fs, 20);
-        mbar_arrive_expect_tx(smem_u32(&m.b_full), 2 * b_half);
-        const int row0 = static_cast<int>((static_cast<size_t>(t) * nbmax + b) * spr);
-        const uint64_t pol = l2_evict_first();
-        tma_load_2d_hint(sbase + kOffB, &tm_spb, 0, row0, smem_u32(&m.b_full), pol);
-        tma_load_2d_hint(sbase + kOffB + b_half, &tm_spb, 64, row0, smem_u32(&m.b_full), pol);
-        for (int n = 0; n < kNT; ++n) {
-          const int u = b * kNT + n, st = u & 1, use = u >> 1;
-          if (use > 0) mbar_wait(smem_u32(&m.a_empty[st]), (use - 1) & 1, fs, 21);
-          const uint32_t base = sbase + kOffA + st * kAStage;
-          const int nd = n < 4 ? 2 : 1;  // 64-d boxes in this chunk
-          const uint32_t bytes = (n < 4 ? 4u : 1u) * box_heads * 128u;
-          mbar_arrive_expect_tx(smem_u32(&m.a_full[st]), bytes);
-          for (int k = 0; k < nd; ++k)
-            tma_load_3d(base + k * a_half, &tm_qa, n * 128 + k * 64, 0, t, smem_u32(&m.a_full[st]));
-          if (n < 4)
-            for (int k = 0; k < 2; ++k)
-              tma_load_3d(base + (2 + k) * a_half, &tm_doa, n * 128 + k * 64, 0, t,
+      int gb = 0;  // blocks so far
+      for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        const int Kt = count[t];
+        if (Kt == 0) continue;
+        const int nblk = (Kt + kBlk - 1) / kBlk;
+        for (int b = 0; b < nblk; ++b, ++gb) {
+          if (gb > 0) mbar_wait(smem_u32(&m.b_empty), (gb - 1) & 1, fs, 20);
+          mbar_arrive_expect_tx(smem_u32(&m.b_full), 2 * b_half);
+          const int row0 = static_cast<int>((static_cast<size_t>(t) * nbmax + b) * spr);
+          const uint64_t pol = l2_evict_first();
+          tma_load_2d_hint(sbase + kOffB, &tm_spb, 0, row0, smem_u32(&m.b_full), pol);
+          tma_load_2d_hint(sbase + kOffB + b_half, &tm_spb, 64, row0, smem_u32(&m.b_full), pol);
+          for (int n = 0; n < kNT; ++n) {
+            const int u = gb * kNT + n, st = u & 1, use = u >> 1;
+            if (use > 0) mbar_wait(smem_u32(&m.a_empty[st]), (use - 1) & 1, fs, 21);
+            const uint32_t base = sbase + kOffA + st * kAStage;
+            const int nd = n < 4 ? 2 : 1;  // 64-d boxes in this chunk
+            const uint32_t bytes = (n < 4 ? 4u : 1u) * box_heads * 128u;
+            mbar_arrive_expect_tx(smem_u32(&m.a_full[st]), bytes);
+            for (int k = 0; k < nd; ++k)
+              tma_load_3d(base + k * a_half, &tm_qa, n * 128 + k * 64, 0, t,
                           smem_u32(&m.a_full[st]));
+            if (n < 4)
+              for (int k = 0; k < 2; ++k)
+                tma_load_3d(base + (2 + k) * a_half, &tm_doa, n * 128 + k * 64, 0, t,
+                            smem_u32(&m.a_full[st]));
+          }
         }
       }
     }
@@ -722,36 +729,44 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       const uint32_t id = idesc_bf16(128, kBlk, true, true);
-      for (int b = 0; b < nblk; ++b) {
-        mbar_wait(smem_u32(&m.b_full), b & 1, fs, 22);
-        for (int n = 0; n < kNT; ++n) {
-          const int u = b * kNT + n, st = u & 1, use = u >> 1;
-          mbar_wait(smem_u32(&m.a_full[st]), use & 1, fs, 23);
-          if (use > 0) mbar_wait(smem_u32(&m.d_empty[st]), (use - 1) & 1, fs, 24);
-          tc_fence_after();
-          const uint32_t base = sbase + kOffA + st * kAStage;
-          const uint32_t d_t = tmem + st * kBlk;
-          // dS' . Q part: A = Q^T (M = d), B = scratch rows 0..HP-1
-          for (int kk = 0; kk < HP / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(base + kk * 2048, a_half, 1024);
-            const uint64_t bb = sdesc_sw128(sbase + kOffB + kk * 2048, b_half, 1024);
-            umma_ss(d_t, a, bb, id, kk != 0);
-          }
-          if (n < 4) {  // P . dO part: A = dO^T, B = scratch rows HP..2HP-1
+      int gb = 0;
+      for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        const int Kt = count[t];
+        if (Kt == 0) continue;
+        const int nblk = (Kt + kBlk - 1) / kBlk;
+        for (int b = 0; b < nblk; ++b, ++gb) {
+          mbar_wait(smem_u32(&m.b_full), gb & 1, fs, 22);
+          for (int n = 0; n < kNT; ++n) {
+            const int u = gb * kNT + n, st = u & 1, use = u >> 1;
+            mbar_wait(smem_u32(&m.a_full[st]), use & 1, fs, 23);
+            if (use > 0) mbar_wait(smem_u32(&m.d_empty[st]), (use - 1) & 1, fs, 24);
+            tc_fence_after();
+            const uint32_t base = sbase + kOffA + st * kAStage;
+            const uint32_t d_t = tmem + st * kBlk;
+            // dS' . Q part: A = Q^T (M = d), B = scratch rows 0..HP-1
             for (int kk = 0; kk < HP / 16; ++kk) {
-              const uint64_t a = sdesc_sw128(base + 2 * a_half + kk * 2048, a_half, 1024);
-              const uint64_t bb =
-                  sdesc_sw128(sbase + kOffB + HP * 128 + kk * 2048, b_half, 1024);
-              umma_ss(d_t, a, bb, id, 1);
+              const uint64_t a = sdesc_sw128(base + kk * 2048, a_half, 1024);
+              const uint64_t bb = sdesc_sw128(sbase + kOffB + kk * 2048, b_half, 1024);
+              umma_ss(d_t, a, bb, id, kk != 0);
             }
+            if (n < 4) {  // P . dO part: A = dO^T, B = scratch rows HP..2HP-1
+              for (int kk = 0; kk < HP / 16; ++kk) {
+                const uint64_t a = sdesc_sw128(base + 2 * a_half + kk * 2048, a_half, 1024);
+                const uint64_t bb =
+                    sdesc_sw128(sbase + kOffB + HP * 128 + kk * 2048, b_half, 1024);
+                umma_ss(d_t, a, bb, id, 1);
+              }
+            }
+            umma_commit(smem_u32(&m.a_empty[st]));
+            umma_commit(smem_u32(&m.d_full[st]));
           }
-          umma_commit(smem_u32(&m.a_empty[st]));
-          umma_commit(smem_u32(&m.d_full[st]));
+          umma_commit(smem_u32(&m.b_empty));
         }
-        umma_commit(smem_u32(&m.b_empty));
       }
-      umma_commit(smem_u32(&m.mma_done));
-      mbar_wait_final<&g_err_bwd>(smem_u32(&m.mma_done), 0);
+      if (gb > 0) {  // all MMAs retired before the TMEM is freed
+        umma_commit(smem_u32(&m.mma_done));
+        mbar_wait_final<&g_err_bwd>(smem_u32(&m.mma_done), 0);
+      }
     }
     __syncwarp();
   } else {
@@ -760,60 +775,66 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
     // slot columns 32 (w / 4) .. +31.
     const int sp = warp & 3, quarter = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
-    const int32_t* rows = idxc + static_cast<size_t>(t) * W;
     const uint64_t keep = l2_evict_last();
-    for (int b = 0; b < nblk; ++b) {
-      const int s0 = b * kBlk + quarter * 32;
-      const int nvalid = max(0, min(32, Kt - s0));
-      // Lane s holds the accumulator offset of slot s0 + s; shuffles hand it
-      // to the whole warp without a shared-memory round trip per add.
-      const uint32_t roff = lane < nvalid ? static_cast<uint32_t>(rows[s0 + lane]) * kD : 0u;
-      for (int n = 0; n < kNT; ++n) {
-        const int u = b * kNT + n, st = u & 1, use = u >> 1;
-        mbar_wait(smem_u32(&m.d_full[st]), use & 1, fs, 25);
-        tc_fence_after();
-        uint32_t v[32];
-        tmem_ld32_sync(tmem + lane_base + st * kBlk + quarter * 32, v);
-        tc_fence_before();
-        mbar_arrive(smem_u32(&m.d_empty[st]));
-        const int d = n * 128 + sp * 32 + lane;
-        if (kDet && (n < 4 || d < kD)) {
-          {
-            unsigned long long* dst = static_cast<unsigned long long*>(dkv_acc) + d;
+    int gb = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+      const int Kt = count[t];
+      if (Kt == 0) continue;
+      const int nblk = (Kt + kBlk - 1) / kBlk;
+      const int32_t* rows = idxc + static_cast<size_t>(t) * W;
+      for (int b = 0; b < nblk; ++b, ++gb) {
+        const int s0 = b * kBlk + quarter * 32;
+        const int nvalid = max(0, min(32, Kt - s0));
+        // Lane s holds the accumulator offset of slot s0 + s; shuffles hand it
+        // to the whole warp without a shared-memory round trip per add.
+        const uint32_t roff = lane < nvalid ? static_cast<uint32_t>(rows[s0 + lane]) * kD : 0u;
+        for (int n = 0; n < kNT; ++n) {
+          const int u = gb * kNT + n, st = u & 1, use = u >> 1;
+          mbar_wait(smem_u32(&m.d_full[st]), use & 1, fs, 25);
+          tc_fence_after();
+          uint32_t v[32];
+          tmem_ld32_sync(tmem + lane_base + st * kBlk + quarter * 32, v);
+          tc_fence_before();
+          mbar_arrive(smem_u32(&m.d_empty[st]));
+          const int d = n * 128 + sp * 32 + lane;
+          if (kDet && (n < 4 || d < kD)) {
+            {
+              unsigned long long* dst = static_cast<unsigned long long*>(dkv_acc) + d;
 #pragma unroll
-            for (int s = 0; s < 32; ++s) {
-              const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
-              if (s < nvalid) red_add_fixed32(dst + o, __uint_as_float(v[s]), keep);
+              for (int s = 0; s < 32; ++s) {
+                const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
+                if (s < nvalid) red_add_fixed32(dst + o, __uint_as_float(v[s]), keep);
+              }
+            }
+          }
+          if constexpr (!kDet) {
+            // The quarter's four warps hold d rows 32 sp .. of the tile for the
+            // same 32 slots.  Through shared memory, 16 slots at a time, each
+            // warp then adds whole 128-float rows: 4 slots per warp, 32 lanes x
+            // 4 floats each (the fast reduction pattern).
+            float* stg = reinterpret_cast<float*>(smem + dkv::kOffStage) + quarter * (16 * 128);
+            const int dt = n * 128;  // first d of the tile
+            const bool lane_ok = dt + lane * 4 < kD;  // the rope tile has 64 columns
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+              for (int s = 0; s < 16; ++s) stg[s * 128 + sp * 32 + lane] = __uint_as_float(v[half * 16 + s]);
+              named_bar_sync(1 + quarter, 128);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int sl = sp * 4 + j;            // slot within the half
+                const int s = half * 16 + sl;         // slot within the quarter
+                const float4 f = *reinterpret_cast<const float4*>(stg + sl * 128 + lane * 4);
+                const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
+                if (s < nvalid && lane_ok)
+                  red_add_v4_f32_hint(static_cast<float*>(dkv_acc) + o + dt + lane * 4, f, keep);
+              }
+              named_bar_sync(1 + quarter, 128);
             }
           }
         }
-        if constexpr (!kDet) {
-          // The quarter's four warps hold d rows 32 sp .. of the tile for the
-          // same 32 slots.  Through shared memory, 16 slots at a time, each
-          // warp then adds whole 128-float rows: 4 slots per warp, 32 lanes x
-          // 4 floats each (the fast reduction pattern).
-          float* stg = reinterpret_cast<float*>(smem + dkv::kOffStage) + quarter * (16 * 128);
-          const int dt = n * 128;  // first d of the tile
-          const bool lane_ok = dt + lane * 4 < kD;  // the rope tile has 64 columns
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int s = 0; s < 16; ++s) stg[s * 128 + sp * 32 + lane] = __uint_as_float(v[half * 16 + s]);
-            named_bar_sync(1 + quarter, 128);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int sl = sp * 4 + j;            // slot within the half
-              const int s = half * 16 + sl;         // slot within the quarter
-              const float4 f = *reinterpret_cast<const float4*>(stg + sl * 128 + lane * 4);
-              const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
-              if (s < nvalid && lane_ok)
-                red_add_v4_f32_hint(static_cast<float*>(dkv_acc) + o + dt + lane * 4, f, keep);
-            }
-            named_bar_sync(1 + quarter, 128);
-          }
-        }
+        __syncwarp();
       }
-      __syncwarp();
     }
   }
 
@@ -964,7 +985,11 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     if (e != cudaSuccess) return e;
     auto kern = p.d_qk == 512 ? (p.deterministic ? k_bwd_dkv<true, 512> : k_bwd_dkv<false, 512>)
                               : (p.deterministic ? k_bwd_dkv<true, 576> : k_bwd_dkv<false, 576>);
-    kern<<<static_cast<unsigned>(p.T), dkv::kThreads, dkv::kSmemBytes, s>>>(
+    // One CTA per token lets the hardware balance the uneven token costs
+    // (measured faster for the fp32 path); the int64 path gains more from
+    // persistent CTAs that prefetch the next token.
+    const int grid = p.deterministic && p.T > sm_count() ? sm_count() : p.T;
+    kern<<<grid, dkv::kThreads, dkv::kSmemBytes, s>>>(
         tm_qa, tm_doa, tm_sp_ld, idxc, count, acc, p.T, p.H, p.W, G, box_all, nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
