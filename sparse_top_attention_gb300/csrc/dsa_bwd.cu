@@ -162,30 +162,38 @@ k_bwd_pre(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict
 
 // ------------------------------------------------------------------ b2-b4: dq, dS', P
 
-constexpr int kHG = 64;                  // heads per item (UMMA N of S and dP each, and of dQ)
-constexpr int kSoftmax = 256;            // warps 0-7: row (warp & 3) * 32 + lane, heads 32 * (warp >> 2) + 0..31
+constexpr int kSoftmax = 256;            // warps 0-7: row (warp & 3) * 32 + lane, half (warp >> 2) of the heads
 constexpr int kMmaWarp = 8;
 constexpr int kIssuer = 288;             // lane 0 of warp 9
 constexpr int kProducers = 96;           // warps 9-11
 constexpr int kLoaderWarp = 12;          // lane 0 streams the (Q, dO) chunk pairs
 constexpr int kThreads = kSoftmax + 32 + kProducers + 32;
 constexpr int kKVChunk = kBlk * 128;     // 16 KB
-constexpr int kHChunk = kHG * 128;       // 8 KB: 64 columns of 64 head rows
-constexpr int kStage = 2 * kHChunk;      // Q chunk x (rows 0..63), then dO chunk x (rows 64..127)
-constexpr int kStages = 4;               // ring of (Q, dO) chunk pairs
-
-// TMEM: [S^T | dP^T] (2 x 64 columns), then dQ^T (5 tiles x 64 columns).
+constexpr int kMaxStages = 8;
+constexpr int kMaxHG = 64;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColdP = 64, kColdQ = 128;
+
+// Head group of an item: 64 heads, or 32 when H <= 32 (less padding: the
+// Q/dO ring stages halve and the MMAs narrow).
+template <int kHG>
+struct DqHeads {
+  static_assert(kHG == 64 || kHG == 32, "head group");
+  static constexpr int kHT = kHG / 2;          // heads per softmax thread
+  static constexpr int kHChunk = kHG * 128;    // 64 columns of kHG head rows
+  static constexpr int kStage = 2 * kHChunk;   // Q chunk x (rows 0..kHG-1), then dO chunk x
+  static constexpr int kStages = kHG == 64 ? 4 : 8;  // ring of (Q, dO) chunk pairs
+  // TMEM: [S^T | dP^T] (2 x kHG columns), then dQ^T (5 tiles x kHG columns).
+  static constexpr uint32_t kColS = 0, kColdP = kHG, kColdQ = 2 * kHG;
+};
 
 struct Misc {
   uint64_t kv_full[kChunks];
   uint64_t kv_free[kChunks];
-  uint64_t qd_full[kStages], qd_free[kStages];
+  uint64_t qd_full[kMaxStages], qd_free[kMaxStages];
   uint64_t s_full, ds_full, rope_done, dsp_free, dq_full, mma_done;
   // per head of the item: (log2(gate) - lse * log2(e), delta), so that
   // P = exp2(s * scale * log2(e) + x) and one 16-byte load serves two heads
-  alignas(16) float2 cd[kHG];
+  alignas(16) float2 cd[kMaxHG];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -196,10 +204,12 @@ struct Misc {
 // of dQ is done), p = 1..8 the V chunks 0..7; blocks are gathered and
 // consumed in the order p = 1..8, 0 because position 0 is released last.
 // Without one, position p holds V chunk p and P has a tile of its own.
-// Q and dO do not stay resident for 64 heads: their chunk x comes in by TMA
-// into a ring stage for each S / dP step.
-template <int kD>
+// Q and dO do not stay resident: their chunk x comes in by TMA into a ring
+// stage for each S / dP step.
+template <int kD, int kHG>
 struct DqLayout {
+  using Hd = DqHeads<kHG>;
+  static constexpr int kHChunk = Hd::kHChunk, kStage = Hd::kStage, kStages = Hd::kStages;
   static constexpr int kCh = kD / 64;
   static constexpr bool kRope = kCh > 8;
   static constexpr int kDT = (kD + 127) / 128;   // 128-row d tiles of dQ^T
@@ -234,13 +244,15 @@ __device__ __forceinline__ int pos_of_step(int i) {
   return kRope ? (i == kChunks - 1 ? 0 : i + 1) : i;
 }
 
-// Byte offset of element (head row h, slot) in a [64 rows x 128 slots] bf16
+// Byte offset of element (head row h, slot) in a [kHG rows x 128 slots] bf16
 // tile kept as two 128B-swizzled sub-tiles of 64 slots: the layout of dS' and
 // P (K-major B for dQ^T; stored to the scratch by TMA, 32 rows x 64 slots
 // per box).
+template <int kHG>
 __device__ __forceinline__ uint32_t hs_tile_off(uint32_t h, uint32_t slot) {
   const uint32_t col = slot & 63u;
-  return (slot >> 6) * kHChunk + h * 128u + ((((col >> 3) ^ (h & 7u)) << 4) | ((col & 7u) << 1));
+  return (slot >> 6) * (kHG * 128u) + h * 128u +
+         ((((col >> 3) ^ (h & 7u)) << 4) | ((col & 7u) << 1));
 }
 
 __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v) {
@@ -249,7 +261,7 @@ __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v) {
 
 // Items are (token, 64-head group) pairs; the scratch keeps its rows per
 // 32-head group (G32 groups: dS' rows first, then P rows).
-template <int kD>
+template <int kD, int kHG>
 __global__ void __launch_bounds__(kThreads, 1)
 k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
          const __grid_constant__ CUtensorMap tm_sp, const __grid_constant__ CUtensorMap tm_kv,
@@ -258,9 +270,12 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
          const float* __restrict__ lse2_g, const float* __restrict__ gate_g,
          const float* __restrict__ delta_g, __nv_bfloat16* __restrict__ dq, int T, int H, int W,
          float scale, int G, int G32, int box_heads, int nbmax) {
-  using L = DqLayout<kD>;
+  using L = DqLayout<kD, kHG>;
+  using Hd = DqHeads<kHG>;
   constexpr int kCh = L::kCh, kDT = L::kDT, kOffKV = L::kOffKV, kOffQD = L::kOffQD,
                 kOffdS = L::kOffdS, kOffP = L::kOffP, kOffMisc = L::kOffMisc;
+  constexpr int kHChunk = Hd::kHChunk, kStage = Hd::kStage, kStages = Hd::kStages, kHT = Hd::kHT;
+  constexpr uint32_t kColS = Hd::kColS, kColdP = Hd::kColdP, kColdQ = Hd::kColdQ;
   constexpr bool kRope = L::kRope;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -476,11 +491,11 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   } else {
     // ------------------------------------------------------------ P, dS', dq
     // Thread (warp w, lane l) owns gathered row (w & 3) * 32 + l of the
-    // block (its TMEM lane) and heads hb .. hb + 31, hb = 32 * (w >> 2): two
+    // block (its TMEM lane) and heads hb .. hb + kHT - 1, hb = kHT * (w >> 2): two
     // warps per SM sub-partition share the exp2 / FMA work of a block.
     const float sl2 = scale * kLog2e;
     const size_t spr = static_cast<size_t>(64) * G32;  // scratch rows per (token, block)
-    const int row = (warp & 3) * 32 + lane, hb = (warp >> 2) * 32;
+    const int row = (warp & 3) * 32 + lane, hb = (warp >> 2) * kHT;
     int it = 0, gb = 0;
     for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
       const int t = u / G, h0 = (u - t * G) * kHG;
@@ -508,13 +523,16 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         mbar_wait(smem_u32(&m.s_full), gb & 1, fs, 7);
         tc_fence_after();
         const bool valid = b * kBlk + row < Kt;
-        uint32_t rs[32], rd[32];
-        tmem_ld32x2_sync(tmem + lane_base + kColS + hb, rs, tmem + lane_base + kColdP + hb, rd);
-        float dsv[32];
-        uint32_t pk[16];  // P as bf16 pairs (heads hb + 2i, hb + 2i + 1)
+        uint32_t rs[kHT], rd[kHT];
+        if constexpr (kHT == 32)
+          tmem_ld32x2_sync(tmem + lane_base + kColS + hb, rs, tmem + lane_base + kColdP + hb, rd);
+        else
+          tmem_ld16x2_sync(tmem + lane_base + kColS + hb, rs, tmem + lane_base + kColdP + hb, rd);
+        float dsv[kHT];
+        uint32_t pk[kHT / 2];  // P as bf16 pairs (heads hb + 2i, hb + 2i + 1)
         const float4* cd4 = reinterpret_cast<const float4*>(m.cd + hb);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
+        for (int i = 0; i < kHT; i += 2) {
           const float4 c = cd4[i / 2];  // heads hb + i, hb + i + 1
           // Live columns satisfy s - lse <= 0, so exp2 never overflows here;
           // rows past the valid count hold zero KV (finite dP) and get P = 0.
@@ -528,9 +546,9 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         // thread 0 finished reading the previous block's tiles out (bulk wait below)
         named_bar_sync(1, kSoftmax);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < kHT; ++i) {
           const __nv_bfloat16 v = __float2bfloat16_rn(dsv[i]);
-          st_shared_b16(sbase + kOffdS + hs_tile_off(hb + i, row),
+          st_shared_b16(sbase + kOffdS + hs_tile_off<kHG>(hb + i, row),
                         *reinterpret_cast<const uint16_t*>(&v));
         }
         fence_proxy_async_smem();
@@ -540,9 +558,10 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         // has read the rope rows.
         if constexpr (kRope) mbar_wait(smem_u32(&m.rope_done), gb & 1, fs, 9);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          st_shared_b16(sbase + kOffP + hs_tile_off(hb + 2 * i, row), static_cast<uint16_t>(pk[i]));
-          st_shared_b16(sbase + kOffP + hs_tile_off(hb + 2 * i + 1, row),
+        for (int i = 0; i < kHT / 2; ++i) {
+          st_shared_b16(sbase + kOffP + hs_tile_off<kHG>(hb + 2 * i, row),
+                        static_cast<uint16_t>(pk[i]));
+          st_shared_b16(sbase + kOffP + hs_tile_off<kHG>(hb + 2 * i + 1, row),
                         static_cast<uint16_t>(pk[i] >> 16));
         }
         fence_proxy_async_smem();
@@ -571,11 +590,14 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       __nv_bfloat16* dq_t = dq + (static_cast<size_t>(t) * H + h0) * kD;
       for (int j = 0; j < kDT; ++j) {
         const int d = j * 128 + row;
-        uint32_t v[32];
-        tmem_ld32_sync(tmem + lane_base + kColdQ + j * kHG + hb, v);
+        uint32_t v[kHT];
+        if constexpr (kHT == 32)
+          tmem_ld32_sync(tmem + lane_base + kColdQ + j * kHG + hb, v);
+        else
+          tmem_ld16_sync(tmem + lane_base + kColdQ + j * kHG + hb, v);
         if (d < kD) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < kHT; ++i) {
             const int h = hb + i;
             if (h < nh) dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(__uint_as_float(v[i]));
           }
@@ -908,12 +930,18 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
                        cudaStream_t s, int stages) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<576>,
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<576, 64>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DqLayout<576>::kSmemBytes);
+                                         DqLayout<576, 64>::kSmemBytes);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_bwd_dq<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               DqLayout<512>::kSmemBytes);
+      e = cudaFuncSetAttribute(k_bwd_dq<512, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DqLayout<512, 64>::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_bwd_dq<576, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DqLayout<576, 32>::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_bwd_dq<512, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DqLayout<512, 32>::kSmemBytes);
     void (*dkv_kernels[])(CUtensorMap, CUtensorMap, CUtensorMap, const int32_t*, const int32_t*,
                           void*, int, int, int, int, int, int) = {
         k_bwd_dkv<false, 576>, k_bwd_dkv<true, 576>, k_bwd_dkv<false, 512>, k_bwd_dkv<true, 512>};
@@ -950,18 +978,24 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
   }
   if ((stages & kBwdMain) && p.T > 0) {
     const int G32 = bwd_groups(p.H), nbmax = bwd_nbmax(p.W);
-    const int G = (p.H + kHG - 1) / kHG;  // 64-head items
+    // 64-head items, or 32-head items when that is all there is
+    const int hg = p.H <= 32 ? 32 : 64;
+    const int G = (p.H + hg - 1) / hg;
     __nv_bfloat16* sp = reinterpret_cast<__nv_bfloat16*>(base + L.sp);
     const long long sp_rows = static_cast<long long>(p.T) * nbmax * 64 * G32;
     CUtensorMap tm_q, tm_do, tm_sp_st, tm_kv;
-    const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
+    const int box_heads = p.H < hg ? p.H : hg;  // never larger than the tensor
     e = make_head_tile_map(&tm_q, q, p.T, p.H, p.d_qk, box_heads);
     if (e == cudaSuccess) e = make_head_tile_map(&tm_do, dout, p.T, p.H, kDv, box_heads);
     if (e == cudaSuccess) e = make_matrix_map(&tm_sp_st, sp, sp_rows, kBlk, 32);
     if (e == cudaSuccess) e = make_matrix_map(&tm_kv, kv, p.S_kv, p.d_qk, kBlk);
     if (e != cudaSuccess) return e;
-    auto kern = p.d_qk == 512 ? k_bwd_dq<512> : k_bwd_dq<576>;
-    const int smem = p.d_qk == 512 ? DqLayout<512>::kSmemBytes : DqLayout<576>::kSmemBytes;
+    auto kern = hg == 32 ? (p.d_qk == 512 ? k_bwd_dq<512, 32> : k_bwd_dq<576, 32>)
+                         : (p.d_qk == 512 ? k_bwd_dq<512, 64> : k_bwd_dq<576, 64>);
+    const int smem = hg == 32 ? (p.d_qk == 512 ? DqLayout<512, 32>::kSmemBytes
+                                               : DqLayout<576, 32>::kSmemBytes)
+                              : (p.d_qk == 512 ? DqLayout<512, 64>::kSmemBytes
+                                               : DqLayout<576, 64>::kSmemBytes);
     // persistent: at most one CTA per SM, each walking its share of the items
     const long long items = static_cast<long long>(p.T) * G;
     const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
