@@ -5,8 +5,9 @@
 //   k_compact   a1: valid KV rows of every token, in slot order, and counts
 //   k_bwd_pre   b1: delta = rowsum(dout * out), lse*log2(e), gate and the
 //               per-(t,h) d_sink terms (FlashAttention "dpsum" preprocess)
-//   k_bwd_dq    b2-b5: per (token, 64-head group) recompute P, form dS,
-//               accumulate dQ in TMEM and store dq; write the dS' and P
+//   k_bwd_dq    b2-b5: per (token, 64-head group; 32 heads when H <= 32)
+//               recompute P, form dS, accumulate dQ in TMEM and store dq;
+//               write the dS' and P
 //               tiles of every 128-slot block to a bf16 scratch.  One
 //               persistent CTA per SM walks the (token, group) items.
 //   k_bwd_dkv   b6: per token, dKV_blk^T = [Q^T | dO^T] [dS'; P] over all
@@ -38,7 +39,8 @@
 // Rows are D = 576 columns (512 V + 64 rope) or 512 (no rope part); the
 // kernels are templates over D.
 // k_bwd_dq tiles, transposed like the forward: gathered rows are UMMA M
-// (128) and the 64 heads of the group are N.
+// (128) and the 64 heads of the group are N (32 heads, and half the N,
+// when H <= 32).
 //   [S^T | dP^T] = KV_blk . [Q^T | dO^T]  M=128 N=128 K=512, then S^T += rope part (N=64, K=64)
 //   dQ^T += KV_blk^T . dS'^T             ceil(D/128) x (M=128 N=64 K=128)
 // where dS' = scale * dS.  dS'^T and P^T tiles are written to the scratch.
@@ -259,7 +261,7 @@ __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-// Items are (token, 64-head group) pairs; the scratch keeps its rows per
+// Items are (token, kHG-head group) pairs; the scratch keeps its rows per
 // 32-head group (G32 groups: dS' rows first, then P rows).
 template <int kD, int kHG>
 __global__ void __launch_bounds__(kThreads, 1)
