@@ -1,6 +1,7 @@
 """GPU parity at the limits of the sizes: no tokens, one token, the widest and
-narrowest index rows, a single KV row, one head and head counts that leave a
-single real head in the last head group."""
+narrowest index rows, a single KV row, one head, a ragged head group
+(H = 33) and a head count that leaves a single real head in the last
+64-head group of both the forward and the backward (H = 65)."""
 import numpy as np
 import pytest
 import torch
@@ -19,8 +20,8 @@ CASES = [
     ("one_slot_per_token", (64, 16, 200, 1, 1, False)),
     ("one_kv_row", (48, 32, 1, 8, 1, False)),
     ("one_head", (256, 1, 700, 640, 600, False)),
-    ("h33_one_head_in_last_bwd_group", (200, 33, 900, 300, 300, True)),
-    ("h65_one_head_in_last_fwd_group", (200, 65, 900, 300, 300, False)),
+    ("h33_ragged_head_group", (200, 33, 900, 300, 300, True)),
+    ("h65_one_head_in_last_group", (200, 65, 900, 300, 300, False)),
     ("h128", (200, 128, 900, 300, 300, False)),
 ]
 
