@@ -930,8 +930,9 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
                        const int32_t* len, const float* sink, const void* out, const float* lse,
                        const void* dout, void* dq, void* dkv, float* dsink, void* ws,
                        cudaStream_t s, int stages) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<uint64_t> attr_done{0};
+  const int dev = current_device();
+  if (device_needs_setup(attr_done, dev)) {
     cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<576, 64>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DqLayout<576, 64>::kSmemBytes);
@@ -951,7 +952,7 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    mark_device_setup(attr_done, dev);
   }
   const BwdWorkspace L = bwd_workspace_layout(p);
   uint8_t* base = static_cast<uint8_t*>(ws);

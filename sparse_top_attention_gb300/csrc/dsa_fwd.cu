@@ -493,8 +493,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
 cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const int32_t* idx,
                        const int32_t* len, const float* sink, void* out, float* lse,
                        cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<uint64_t> attr_done{0};
+  const int dev = current_device();
+  if (device_needs_setup(attr_done, dev)) {
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel<576>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          FwdLayout<576>::kSmemBytes);
@@ -502,7 +503,7 @@ cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const in
       e = cudaFuncSetAttribute(fwd_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                FwdLayout<512>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    mark_device_setup(attr_done, dev);
   }
   const int G = (p.H + kHG - 1) / kHG;
   const long long items = static_cast<long long>(p.T) * G;

@@ -1,6 +1,7 @@
 // Launchers shared between the kernel translation units and the C-ABI layer.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -34,6 +35,20 @@ struct BwdWorkspace {
                     // contiguous; G = ceil(H / 32), nbmax = ceil(W / 128)
   size_t total;
 };
+// Kernel attributes (the dynamic shared-memory limit) hold per device, so
+// each launcher records in a bitmask which devices it has set up.  Device
+// ordinals past 63 are set up on every call.
+inline int current_device() {
+  int d = 0;
+  return cudaGetDevice(&d) == cudaSuccess ? d : -1;
+}
+inline bool device_needs_setup(const std::atomic<uint64_t>& done, int dev) {
+  return dev < 0 || dev >= 64 || (done.load(std::memory_order_acquire) & (1ull << dev)) == 0;
+}
+inline void mark_device_setup(std::atomic<uint64_t>& done, int dev) {
+  if (dev >= 0 && dev < 64) done.fetch_or(1ull << dev, std::memory_order_release);
+}
+
 // SMs of the current device: the grid size of the persistent kernels.
 inline int sm_count() {
   int dev = 0, n = 0;
