@@ -25,9 +25,10 @@
  *  - Tensors are dense and row-major.  Device pointers are 16-byte aligned,
  *    else DSA_ERR_ALIGNMENT.
  *  - The caller owns every buffer.  The library never allocates device
- *    memory.  Its only host state is set up on first use: each kernel's
- *    shared-memory limit, and the device address of dsa_bwd_no_alloc's
- *    array.  Make a first call before any stream capture.
+ *    memory.  Its only host state is set up on first use on each device:
+ *    each kernel's shared-memory limit, and the device address of
+ *    dsa_bwd_no_alloc's array.  Make a first call on a device before any
+ *    stream capture there.
  *  - All work is queued on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream) and the calls return before it finishes.
  *  - Argument and shape errors are returned before anything is launched.
