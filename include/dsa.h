@@ -28,7 +28,9 @@
  *    memory.  Its only host state is set up on first use on each device:
  *    each kernel's shared-memory limit, and the device address of
  *    dsa_bwd_no_alloc's array.  Make a first call on a device before any
- *    stream capture there.
+ *    stream capture there.  A cudaDeviceReset invalidates that state, and
+ *    the library does not notice it: do not reset a device on which the
+ *    library has been used while the library stays loaded.
  *  - All work is queued on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream) and the calls return before it finishes.
  *  - Argument and shape errors are returned before anything is launched.
@@ -58,7 +60,9 @@ typedef enum {
   DSA_ERR_ALIGNMENT = 3,      /* a device pointer is not 16-byte aligned */
   DSA_ERR_WORKSPACE = 4,      /* workspace missing or too small */
   DSA_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
-  DSA_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up waiting on a barrier */
+  DSA_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up waiting on a barrier */
+  DSA_ERR_RANGE = 7           /* DSA_FLAG_DETERMINISTIC: a dkv row may have
+                                 left the fixed-point accumulator's range */
 } dsa_status_t;
 
 typedef struct {
@@ -73,18 +77,18 @@ typedef struct {
 } dsa_problem_t;
 
 /*
- * DSA_FLAG_DELTA_RESIDUAL: exact delta for the backward.
- * By default the backward forms delta = rowsum(dout * out) from the bf16
- * out, as the pages' kernels do.  The cuDNN page "DSA backward SM90: fix
- * three top-k and attention-sink boundary failures" ("Not addressed")
- * traces the remaining d_sink / dq / dkv error to that rounding and names
- * a forward-side fix.  With this flag, `out` points to 2*T*H*512 bf16
- * values: the rounded output [T, H, 512] followed by its rounding residual
- * bf16(O - bf16(O)) [T, H, 512].
+ * DSA_FLAG_DELTA_RESIDUAL: a forward output that carries about fp32 O.
+ * With this flag, `out` points to 2*T*H*512 bf16 values: the rounded
+ * output [T, H, 512] followed by its rounding residual bf16(O - bf16(O))
+ * [T, H, 512].
  *   - dsa_fwd writes both halves.
- *   - dsa_bwd forms delta from their sum, which carries about 16 bits of
- *     the fp32 O.
- * The flag must be the same in the forward and the backward call.
+ *   - dsa_bwd takes its first delta estimate from their sum.
+ * This is the forward-side fix that the cuDNN page "DSA backward SM90: fix
+ * three top-k and attention-sink boundary failures" ("Not addressed") names
+ * for the delta error of a bf16 out.  The backward no longer needs it: it
+ * forms the exact delta itself (see dsa_bwd), so the flag only shrinks the
+ * correction it applies.  The flag must be the same in the forward and the
+ * backward call.
  */
 #define DSA_FLAG_DELTA_RESIDUAL 1u
 
@@ -98,8 +102,16 @@ typedef struct {
  * same bits every run; dq and d_sink are deterministic in both modes.
  *   - Resolution 2^-32 (2.3e-10) per add; every dkv element must stay
  *     below 2^31 in magnitude.
+ *   - Range check: every element of KV row r receives n_r adds (the valid
+ *     slots naming r), each at most m_r in magnitude, so its sum is bounded
+ *     by n_r * m_r.  The backward counts n_r, tracks m_r, and where
+ *     n_r * m_r reaches 2^31 the row may have wrapped: the call still
+ *     completes, and the next dsa_device_status returns DSA_ERR_RANGE
+ *     (dkv is then not to be trusted).  The bound is conservative: no row
+ *     that passes it can have wrapped.
  *   - The dkv accumulator in the workspace takes 8 bytes per element
- *     instead of 4 (dsa_bwd_workspace_bytes accounts for it).
+ *     instead of 4, plus 8 bytes per KV row for the range check
+ *     (dsa_bwd_workspace_bytes accounts for both).
  * Ignored by dsa_fwd.
  */
 #define DSA_FLAG_DETERMINISTIC 2u
@@ -127,8 +139,8 @@ dsa_status_t dsa_fwd(const dsa_problem_t* problem, const void* q, const void* kv
  *   - the dkv accumulator             [S_kv, D], fp32 (int64 with
  *                                     DSA_FLAG_DETERMINISTIC);
  *   - the compacted index lists       [T, W] and their counts [T];
- *   - per-(t,h) fp32 rows: lse*log2(e), sigma(lse - sink), delta and the
- *     d_sink terms;
+ *   - per-(t,h) fp32 rows: lse*log2(e), sigma(lse - sink), delta, the
+ *     d_sink terms and the delta correction;
  *   - the dS'/P scratch that the main stage writes and the finalize stage
  *     reads: bf16 [T, ceil(W / 128), 64 * ceil(H / 32), 128].
  */
@@ -136,11 +148,8 @@ size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem);
 
 /*
  * Backward of the loss sum(dout * out).  Inputs are as for dsa_fwd, plus:
- *   out    bf16 [T, H, 512]  the forward output; delta = rowsum(dout * out)
- *                            is taken from it (the FlashAttention identity,
- *                            cuDNN page "Not addressed").  With
- *                            DSA_FLAG_DELTA_RESIDUAL: [2, T, H, 512] as
- *                            written by dsa_fwd, and delta uses hi + lo.
+ *   out    bf16 [T, H, 512]  the forward output (with DSA_FLAG_DELTA_RESIDUAL
+ *                            [2, T, H, 512] as written by dsa_fwd)
  *   lse    fp32 [T, H]       the forward's lse
  *   dout   bf16 [T, H, 512]
  * Outputs, all overwritten, never accumulated:
@@ -152,6 +161,13 @@ size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem);
  * The call queues, in order: a memset, slot compaction, the delta
  * preprocess, the dq kernel, the dkv kernel, the dkv cast, and the d_sink
  * reduce.
+ * Delta.  The gradients use the exact delta[t,h] = sum_j P_j dP_j, the
+ * accurate form in the cuDNN page's "Not addressed" table, not only
+ * rowsum(dout * out) of the bf16 out (the FlashAttention identity), whose
+ * rounding the one-hot rows of a saturated softmax turn into dq/dkv error.
+ * No second pass over the top-k is needed: dS is formed with the delta of
+ * out, and since the gradients are linear in delta, the difference is
+ * applied to dq, dkv and d_sink once each token's sum of dS is known.
  */
 dsa_status_t dsa_bwd(const dsa_problem_t* problem, const void* q, const void* kv,
                      const int32_t* topk_idxs, const int32_t* topk_length, const float* sink,
@@ -273,10 +289,26 @@ dsa_status_t dsa_topk_compact(const dsa_problem_t* problem, const int32_t* topk_
  * word.  Returns:
  *   DSA_ERR_DEVICE_TIMEOUT  a kernel gave up waiting on one of its own
  *                           barriers (outputs of that call are garbage);
+ *   DSA_ERR_RANGE           a DSA_FLAG_DETERMINISTIC backward failed its
+ *                           range check (its dkv is not to be trusted);
  *   DSA_ERR_CUDA            the stream reported an error;
  *   DSA_OK                  otherwise.
  */
 dsa_status_t dsa_device_status(void* stream);
+
+/*
+ * Self-test of the bounded waits, for tests of a caller's failure handling;
+ * it computes nothing.  Every wait inside this library's kernels gives up
+ * after a time limit (2 s), records DSA_ERR_DEVICE_TIMEOUT in the library's
+ * device error word and lets the kernel return, so that a lost arrival
+ * never hangs the GPU.  This call queues one small kernel on `stream` with
+ * two waits on barriers that nothing completes: one with a limit of
+ * `limit_us` microseconds (1 .. 1000000, else DSA_ERR_INVALID_ARG), one
+ * with the ordinary limit, which the first one's abort flag ends early.
+ * The next dsa_device_status then returns DSA_ERR_DEVICE_TIMEOUT (and
+ * clears the word); the context stays usable.
+ */
+dsa_status_t dsa_wait_selftest(uint32_t limit_us, void* stream);
 
 /* Static English text for a status code. */
 const char* dsa_status_string(dsa_status_t status);

@@ -53,6 +53,15 @@ dsa_status_t apply_varlen(const dsa_varlen_t* v, dsa::Problem* p) {
 
 }  // namespace
 
+namespace dsa {
+dsa_status_t bwd_workspace_checked(const dsa_problem_t* problem, size_t* bytes) {
+  const dsa_status_t st = check_problem(problem);
+  if (st != DSA_OK) return st;
+  *bytes = bwd_workspace_layout(to_internal(problem)).total;
+  return DSA_OK;
+}
+}  // namespace dsa
+
 extern "C" {
 
 static dsa_status_t fwd_impl(const dsa_problem_t* problem, const dsa_varlen_t* varlen,
@@ -89,8 +98,8 @@ dsa_status_t dsa_fwd_varlen(const dsa_problem_t* problem, const dsa_varlen_t* va
 }
 
 size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem) {
-  if (check_problem(problem) != DSA_OK) return 0;
-  return dsa::bwd_workspace_layout(to_internal(problem)).total;
+  size_t n = 0;
+  return dsa::bwd_workspace_checked(problem, &n) == DSA_OK ? n : 0;
 }
 
 static dsa_status_t bwd_stages(const dsa_problem_t* problem, const void* q, const void* kv,
@@ -155,13 +164,21 @@ dsa_status_t dsa_topk_compact(const dsa_problem_t* problem, const int32_t* topk_
                                        count_out, static_cast<cudaStream_t>(stream)));
 }
 
+dsa_status_t dsa_wait_selftest(uint32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return DSA_ERR_INVALID_ARG;
+  return from_cuda(dsa::launch_wait_selftest(static_cast<uint64_t>(limit_us) * 1000u,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 dsa_status_t dsa_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return DSA_ERR_CUDA;
   const unsigned int a = dsa::fwd_take_error();
   const unsigned int b = dsa::bwd_take_error();
   if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu) return DSA_ERR_CUDA;
-  if (a != 0 || b != 0) return DSA_ERR_DEVICE_TIMEOUT;
+  if (a != 0) return DSA_ERR_DEVICE_TIMEOUT;
+  if (b == dsa::kErrDetRange) return DSA_ERR_RANGE;
+  if (b != 0) return DSA_ERR_DEVICE_TIMEOUT;
   return DSA_OK;
 }
 
@@ -174,6 +191,7 @@ const char* dsa_status_string(dsa_status_t s) {
     case DSA_ERR_WORKSPACE: return "workspace missing or too small";
     case DSA_ERR_CUDA: return "CUDA runtime error";
     case DSA_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on an internal barrier";
+    case DSA_ERR_RANGE: return "a deterministic dkv row may have left the accumulator's range";
   }
   return "unknown status";
 }

@@ -68,12 +68,18 @@ BwdWorkspace bwd_workspace_layout(const Problem& p) {
   size_t off = 0;
   const size_t TH = static_cast<size_t>(p.T) * p.H;
   w.dkv_acc = off; off = up(off + static_cast<size_t>(p.S_kv) * p.d_qk * (p.deterministic ? 8 : 4));
+  if (p.deterministic) {  // the range bound per KV row, zeroed with the accumulator
+    w.det_count = off; off = up(off + static_cast<size_t>(p.S_kv) * 4);
+    w.det_max = off;   off = up(off + static_cast<size_t>(p.S_kv) * 4);
+  }
+  w.zero_bytes = off;
   w.idxc = off;    off = up(off + static_cast<size_t>(p.T) * p.W * 4);
   w.count = off;   off = up(off + static_cast<size_t>(p.T) * 4);
   w.lse2 = off;    off = up(off + TH * 4);
   w.gate = off;    off = up(off + TH * 4);
   w.delta = off;   off = up(off + TH * 4);
   w.dsink_t = off; off = up(off + TH * 4);
+  w.cfix = off;    off = up(off + TH * 4);
   w.sp = off;
   off = up(off + static_cast<size_t>(p.T) * bwd_nbmax(p.W) * 64 * bwd_groups(p.H) * 128 * 2);
   w.total = off;
@@ -88,18 +94,23 @@ __device__ unsigned int g_err_bwd;
 
 constexpr int kCompactThreads = 256;
 
+// With `row_refs` (deterministic mode), also counts how many valid slots name
+// each KV row: the number of adds every element of that row receives.
 __global__ void __launch_bounds__(kCompactThreads)
 k_compact(const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ topk_length,
           int32_t* __restrict__ idx_out, int32_t* __restrict__ count_out, int W, int S_kv,
-          const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv, int B) {
+          const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_kv, int B,
+          unsigned int* __restrict__ row_refs) {
   __shared__ int warp_counts[kCompactThreads / 32];
   const int t = blockIdx.x;
   const int len = slot_len(topk_length, t, W);
   const KvRange kvr = kv_range(cu_q, cu_kv, B, t, S_kv);
-  const int n = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, kvr,
-                              idx_out + static_cast<size_t>(t) * W, W, warp_counts, threadIdx.x,
-                              kCompactThreads);
+  int32_t* list = idx_out + static_cast<size_t>(t) * W;
+  const int n = compact_token(topk_idxs + static_cast<size_t>(t) * W, W, len, kvr, list, W,
+                              warp_counts, threadIdx.x, kCompactThreads);
   if (threadIdx.x == 0) count_out[t] = n;
+  if (row_refs != nullptr)  // the list is complete: compact_token ends on a barrier
+    for (int i = threadIdx.x; i < n; i += kCompactThreads) atomicAdd(row_refs + list[i], 1u);
 }
 
 // ------------------------------------------------------------------ b1
@@ -174,6 +185,7 @@ constexpr int kKVChunk = kBlk * 128;     // 16 KB
 constexpr int kMaxStages = 8;
 constexpr int kMaxHG = 64;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kOnesBytes = 2048;         // bf16 ones: two 8-slot groups of 128-byte rows
 
 // Head group of an item: 64 heads, or 32 when H <= 32 (less padding: the
 // Q/dO ring stages halve and the MMAs narrow).
@@ -184,17 +196,22 @@ struct DqHeads {
   static constexpr int kHChunk = kHG * 128;    // 64 columns of kHG head rows
   static constexpr int kStage = 2 * kHChunk;   // Q chunk x (rows 0..kHG-1), then dO chunk x
   static constexpr int kStages = kHG == 64 ? 4 : 8;  // ring of (Q, dO) chunk pairs
-  // TMEM: [S^T | dP^T] (2 x kHG columns), then dQ^T (5 tiles x kHG columns).
+  // TMEM: [S^T | dP^T] (2 x kHG columns), then dQ^T (kHG columns per 128-row
+  // d tile).  The tile after the four V tiles is the rope tile (D = 576),
+  // 2 x kHG wide: its second half accumulates KV_rope^T . P^T.  At D = 512
+  // the same columns hold sigma, the per-head sum of the stored dS'.
   static constexpr uint32_t kColS = 0, kColdP = kHG, kColdQ = 2 * kHG;
+  static constexpr uint32_t kColTail = kColdQ + 4 * kHG;
 };
 
 struct Misc {
   uint64_t kv_full[kChunks];
   uint64_t kv_free[kChunks];
   uint64_t qd_full[kMaxStages], qd_free[kMaxStages];
-  uint64_t s_full, ds_full, rope_done, dsp_free, dq_full, mma_done;
+  uint64_t s_full, ds_full, dsp_free, dq_full, mma_done;
   // per head of the item: (log2(gate) - lse * log2(e), delta), so that
-  // P = exp2(s * scale * log2(e) + x) and one 16-byte load serves two heads
+  // P = exp2(s * scale * log2(e) + x) and one 16-byte load serves two heads;
+  // in the epilogue: (sigma, c)
   alignas(16) float2 cd[kMaxHG];
   uint32_t tmem_base;
   int abort_flag;
@@ -202,27 +219,38 @@ struct Misc {
 
 // Shared-memory layout for rows of kD columns (576 = 512 V + 64 rope, or 512).
 // With a rope chunk, position p of the gathered block holds d-chunk x(p):
-// p = 0 the rope columns 512..575 (reused for the P tile once the rope part
-// of dQ is done), p = 1..8 the V chunks 0..7; blocks are gathered and
-// consumed in the order p = 1..8, 0 because position 0 is released last.
-// Without one, position p holds V chunk p and P has a tile of its own.
+// p = 0 the rope columns 512..575, p = 1..8 the V chunks 0..7; blocks are
+// gathered and consumed in the order p = 1..8, 0.  Without one, position p
+// holds V chunk p.
 // Q and dO do not stay resident: their chunk x comes in by TMA into a ring
-// stage for each S / dP step.
+// stage for each S / dP step (64-head items with a rope chunk keep three
+// stages, so that P has a tile of its own beside dS').
+// The dS'/P tile is two 64-slot halves, each kHG dS' rows followed by kHG P
+// rows (128B-swizzled, slots contiguous): K-major B of the dQ MMAs (the
+// rope tile reads both row sets as one N = 2 kHG operand) and the source of
+// the scratch stores.
+// The ones tile is the A operand of the rows that sum dS' over the slots:
+// the rope tile's filler rows (D = 576, placed above the KV tile so that
+// every step's LBO reaches it) or a tile of its own (D = 512, placed first).
 template <int kD, int kHG>
 struct DqLayout {
   using Hd = DqHeads<kHG>;
-  static constexpr int kHChunk = Hd::kHChunk, kStage = Hd::kStage, kStages = Hd::kStages;
+  static constexpr int kHChunk = Hd::kHChunk, kStage = Hd::kStage;
   static constexpr int kCh = kD / 64;
   static constexpr bool kRope = kCh > 8;
+  static constexpr int kStages = (kRope && kHG == 64) ? 3 : Hd::kStages;
   static constexpr int kDT = (kD + 127) / 128;   // 128-row d tiles of dQ^T
-  static constexpr int kOffKV = 0;
+  static constexpr int kOffKV = kRope ? 0 : kOnesBytes;
   static constexpr int kOffQD = kOffKV + kCh * kKVChunk;
-  static constexpr int kOffdS = kOffQD + kStages * kStage;  // 2 sub-tiles of 64 slots
-  static constexpr int kOffP = kRope ? kOffKV : kOffdS + 2 * kHChunk;
-  static constexpr int kOffMisc = kRope ? kOffdS + 2 * kHChunk : kOffP + 2 * kHChunk;
+  static constexpr int kOffSP = kOffQD + kStages * kStage;
+  static constexpr int kOffOnes = kRope ? kOffSP + 4 * kHChunk : 0;
+  static constexpr int kOffMisc = kRope ? kOffOnes + kOnesBytes : kOffSP + 4 * kHChunk;
   static constexpr int kSmemBytes = kOffMisc + static_cast<int>(sizeof(Misc));
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kOffQD % 1024 == 0 && kOffdS % 1024 == 0 && kOffP % 1024 == 0, "alignment");
+  static_assert(kOffQD % 1024 == 0 && kOffSP % 1024 == 0 && kOffOnes % 1024 == 0, "alignment");
+  // The rope tile's LBO (filler rows -> ones tile) must fit the descriptor's
+  // 14-bit field of 16-byte units.
+  static_assert(!kRope || kOffOnes - kOffKV < (1 << 18), "LBO range");
 };
 
 template <unsigned int* kErr>
@@ -246,15 +274,15 @@ __device__ __forceinline__ int pos_of_step(int i) {
   return kRope ? (i == kChunks - 1 ? 0 : i + 1) : i;
 }
 
-// Byte offset of element (head row h, slot) in a [kHG rows x 128 slots] bf16
-// tile kept as two 128B-swizzled sub-tiles of 64 slots: the layout of dS' and
-// P (K-major B for dQ^T; stored to the scratch by TMA, 32 rows x 64 slots
-// per box).
+// Byte offset of element (row, slot) of the dS'/P tile: rows 0..kHG-1 are
+// the heads' dS', rows kHG..2 kHG-1 their P; each 64-slot half is a
+// 128B-swizzled [2 kHG rows x 64 slots] tile (stored to the scratch by TMA,
+// 32 rows x 64 slots per box).
 template <int kHG>
-__device__ __forceinline__ uint32_t hs_tile_off(uint32_t h, uint32_t slot) {
+__device__ __forceinline__ uint32_t hs_tile_off(uint32_t r, uint32_t slot) {
   const uint32_t col = slot & 63u;
-  return (slot >> 6) * (kHG * 128u) + h * 128u +
-         ((((col >> 3) ^ (h & 7u)) << 4) | ((col & 7u) << 1));
+  return (slot >> 6) * (2u * kHG * 128u) + r * 128u +
+         ((((col >> 3) ^ (r & 7u)) << 4) | ((col & 7u) << 1));
 }
 
 __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v) {
@@ -263,6 +291,23 @@ __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v) {
 
 // Items are (token, kHG-head group) pairs; the scratch keeps its rows per
 // 32-head group (G32 groups: dS' rows first, then P rows).
+//
+// Exact delta without a second pass.  dS' is formed with delta_a, the delta
+// of the bf16 out (k_bwd_pre).  The exact delta, sum_j P_j dP_j in fp32, is
+// the one the cuDNN page "DSA backward SM90: fix three top-k and
+// attention-sink boundary failures" ("Not addressed") measures as the
+// accurate form; that page notes it needs every P_j dP_j before any dS_j.
+// Here the gradients are linear in delta, so it is applied afterwards:
+//   sigma_h = sum_j dS'_j            (fp32 dS': the MMA sums the stored bf16
+//                                     dS' through rows of a ones tile, and the
+//                                     softmax threads add the bf16 rounding
+//                                     remainders they kept)
+//   c_h     = sigma_h - scale * delta_a * p_sink = scale * (delta - delta_a)
+//   dq      = sum_j dS'_j KV_j - c_h [out, sum_j P_j KV_j[512:]]
+//   dS''_j  = dS'_j - c_h P_j        (k_bwd_dkv, before its dKV GEMM)
+//   dsink  += -p_sink (delta - delta_a)
+// The first-order terms of the bf16 rounding of out drop out, which matters
+// where the attention is one-hot and dS is all rounding noise.
 template <int kD, int kHG>
 __global__ void __launch_bounds__(kThreads, 1)
 k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -270,14 +315,17 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
          const __nv_bfloat16* __restrict__ kv,
          const int32_t* __restrict__ idxc, const int32_t* __restrict__ count,
          const float* __restrict__ lse2_g, const float* __restrict__ gate_g,
-         const float* __restrict__ delta_g, __nv_bfloat16* __restrict__ dq, int T, int H, int W,
+         const float* __restrict__ delta_g, const __nv_bfloat16* __restrict__ out,
+         float* __restrict__ dsink_t, float* __restrict__ cfix_g,
+         __nv_bfloat16* __restrict__ dq, int T, int H, int W,
          float scale, int G, int G32, int box_heads, int nbmax) {
   using L = DqLayout<kD, kHG>;
   using Hd = DqHeads<kHG>;
   constexpr int kCh = L::kCh, kDT = L::kDT, kOffKV = L::kOffKV, kOffQD = L::kOffQD,
-                kOffdS = L::kOffdS, kOffP = L::kOffP, kOffMisc = L::kOffMisc;
-  constexpr int kHChunk = Hd::kHChunk, kStage = Hd::kStage, kStages = Hd::kStages, kHT = Hd::kHT;
-  constexpr uint32_t kColS = Hd::kColS, kColdP = Hd::kColdP, kColdQ = Hd::kColdQ;
+                kOffSP = L::kOffSP, kOffOnes = L::kOffOnes, kOffMisc = L::kOffMisc;
+  constexpr int kHChunk = Hd::kHChunk, kStage = Hd::kStage, kStages = L::kStages, kHT = Hd::kHT;
+  constexpr uint32_t kColS = Hd::kColS, kColdP = Hd::kColdP, kColdQ = Hd::kColdQ,
+                     kColTail = Hd::kColTail;
   constexpr bool kRope = L::kRope;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -305,7 +353,6 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     }
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.ds_full), kSoftmax);
-    mbar_init(smem_u32(&m.rope_done), 1);
     mbar_init(smem_u32(&m.dsp_free), 1);
     mbar_init(smem_u32(&m.dq_full), 1);
     mbar_init(smem_u32(&m.mma_done), 1);
@@ -325,6 +372,11 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
                    : "memory");
     }
   }
+  // The ones tile (bf16 1.0 = 0x3F80).
+  for (int i = tid; i < kOnesBytes / 16; i += kThreads)
+    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sbase + kOffOnes + i * 16),
+                 "r"(0x3F803F80u)
+                 : "memory");
   fence_proxy_async_smem();
   if (warp == kMmaWarp) tmem_alloc(smem_u32(&m.tmem_base), kTmemCols);
   tc_fence_before();
@@ -345,6 +397,9 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         const int t = u / G, h0 = (u - t * G) * kHG;
         const int Kt = count[t];
         if (Kt == 0) continue;
+        // the item's out rows, read by the dq correction at its end
+        bulk_prefetch_l2(out + (static_cast<size_t>(t) * H + h0) * kDv,
+                         static_cast<uint32_t>(min(kHG, H - h0)) * kDv * 2u);
         const int nsteps = (Kt + kBlk - 1) / kBlk * kCh;
         for (int k = 0; k < nsteps; ++k, ++gs) {
           const int x = dchunk_of_pos<kRope>(pos_of_step<kRope>(k % kCh));
@@ -429,6 +484,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       const uint32_t idSdP = idesc_bf16(128, 2 * kHG, false, false);  // [S^T | dP^T]
       const uint32_t idS = idesc_bf16(128, kHG, false, false);         // S^T, rope part
       const uint32_t idQ = idesc_bf16(128, kHG, true, false);  // dQ^T: A MN-major, B K-major
+      const uint32_t idQ2 = idesc_bf16(128, 2 * kHG, true, false);  // rope tile: B = [dS'; P]
       int it = 0, gb = 0, gs = 0;
       for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
         const int t = u / G;
@@ -455,28 +511,38 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
             umma_commit(smem_u32(&m.qd_free[s]));
           }
           umma_commit(smem_u32(&m.s_full));
-          // dS' of this block; for the first block of an item this also
+          // dS' and P of this block; for the first block of an item this also
           // orders the softmax warps' read-out of the previous dQ^T first
           mbar_wait(smem_u32(&m.ds_full), gb & 1, fs, 4);
           tc_fence_after();
-          // dQ^T chunks: rope first (its second 64-row atom reads V chunk 0 as
-          // filler rows that are never stored), then d rows 0..511.
+          // dQ^T chunks: rope first, then d rows 0..511.  The rope tile's B
+          // is [dS'; P] (N = 2 kHG), so its second half accumulates
+          // KV_rope^T . P^T; its 64 filler rows (d 576..639) read the ones
+          // tile, so they accumulate sigma = sum over slots of dS' (and of P).
           for (int jj = 0; jj < kDT; ++jj) {
             const int j = kRope ? ((jj == 0) ? 4 : jj - 1) : jj;
             const int pos0 = (j == 4) ? 0 : (kRope ? 1 + 2 * j : 2 * j);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t a =
-                  sdesc_sw128(sbase + kOffKV + pos0 * kKVChunk + kk * 2048, kKVChunk, 1024);
+              const uint32_t a_addr = kOffKV + pos0 * kKVChunk + kk * 2048;
+              const uint32_t lbo = (j == 4) ? static_cast<uint32_t>(kOffOnes) - a_addr : kKVChunk;
+              const uint64_t a = sdesc_sw128(sbase + a_addr, lbo, 1024);
               const uint64_t bs =
-                  sdesc_sw128(sbase + kOffdS + (kk >> 2) * kHChunk + (kk & 3) * 32, 16, 1024);
-              umma_ss(tmem + kColdQ + j * kHG, a, bs, idQ, (b | kk) != 0);
+                  sdesc_sw128(sbase + kOffSP + (kk >> 2) * (2 * kHChunk) + (kk & 3) * 32, 16, 1024);
+              umma_ss(tmem + kColdQ + j * kHG, a, bs, j == 4 ? idQ2 : idQ, (b | kk) != 0);
             }
-            if (j == 4) {
-              umma_commit(smem_u32(&m.rope_done));
-            } else {
-              umma_commit(smem_u32(&m.kv_free[pos0]));
-              umma_commit(smem_u32(&m.kv_free[pos0 + 1]));
+            umma_commit(smem_u32(&m.kv_free[pos0]));
+            if (j != 4) umma_commit(smem_u32(&m.kv_free[pos0 + 1]));
+          }
+          if constexpr (!kRope) {
+            // sigma without a rope tile: rows 0..63 of A are the ones tile,
+            // rows 64..127 (never read) the first dS' rows.
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t a = sdesc_sw128(sbase + kOffOnes, kOffSP - kOffOnes, 1024);
+              const uint64_t bs =
+                  sdesc_sw128(sbase + kOffSP + (kk >> 2) * (2 * kHChunk) + (kk & 3) * 32, 16, 1024);
+              umma_ss(tmem + kColTail, a, bs, idQ, (b | kk) != 0);
             }
           }
           umma_commit(smem_u32(&m.dsp_free));
@@ -512,15 +578,23 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         continue;
       }
       const int nblk = (Kt + kBlk - 1) / kBlk;
+      float gate_h = 0.f, dsink_h = 0.f;  // thread tid < nh: head h0 + tid, for the epilogue
       if (tid < kHG) {
         // Padded heads get gate 0, hence P = dS = 0: they add nothing anywhere.
         const bool real = tid < nh;
         const size_t r = static_cast<size_t>(t) * H + h0 + tid;
-        const float gt = real ? gate_g[r] : 0.f;
-        m.cd[tid] = make_float2(gt > 0.f ? log2f(gt) - lse2_g[r] : -INFINITY,
+        gate_h = real ? gate_g[r] : 0.f;
+        dsink_h = real ? dsink_t[r] : 0.f;
+        m.cd[tid] = make_float2(gate_h > 0.f ? log2f(gate_h) - lse2_g[r] : -INFINITY,
                                 real ? delta_g[r] : 0.f);
       }
       named_bar_sync(1, kSoftmax);
+      // Per head, this row's sum over the item's blocks of the bf16 rounding
+      // remainder of dS' (dS' - bf16(dS')): sigma from the MMA sums the
+      // stored bf16 values, and these remainders bring it to fp32 accuracy.
+      __nv_bfloat162 eacc[kHT / 2];
+#pragma unroll
+      for (int i = 0; i < kHT / 2; ++i) eacc[i] = __float2bfloat162_rn(0.f);
       for (int b = 0; b < nblk; ++b, ++gb) {
         mbar_wait(smem_u32(&m.s_full), gb & 1, fs, 7);
         tc_fence_after();
@@ -544,29 +618,34 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
           dsv[i + 1] = p1 * (__uint_as_float(rd[i + 1]) - c.w) * scale;
           pk[i / 2] = pack_bf16x2(p0, p1);
         }
+        uint32_t dk[kHT / 2];  // dS' as bf16 pairs
+#pragma unroll
+        for (int i = 0; i < kHT; i += 2) {
+          dk[i / 2] = pack_bf16x2(dsv[i], dsv[i + 1]);
+          const float r0 = dsv[i] - __uint_as_float(dk[i / 2] << 16);
+          const float r1 = dsv[i + 1] - __uint_as_float(dk[i / 2] & 0xFFFF0000u);
+          eacc[i / 2] = __hadd2(eacc[i / 2], __floats2bfloat162_rn(r0, r1));
+        }
         if (gb > 0) mbar_wait(smem_u32(&m.dsp_free), (gb - 1) & 1, fs, 8);
         // thread 0 finished reading the previous block's tiles out (bulk wait below)
         named_bar_sync(1, kSoftmax);
 #pragma unroll
-        for (int i = 0; i < kHT; ++i) {
-          const __nv_bfloat16 v = __float2bfloat16_rn(dsv[i]);
-          st_shared_b16(sbase + kOffdS + hs_tile_off<kHG>(hb + i, row),
-                        *reinterpret_cast<const uint16_t*>(&v));
+        for (int i = 0; i < kHT / 2; ++i) {
+          st_shared_b16(sbase + kOffSP + hs_tile_off<kHG>(hb + 2 * i, row),
+                        static_cast<uint16_t>(dk[i]));
+          st_shared_b16(sbase + kOffSP + hs_tile_off<kHG>(hb + 2 * i + 1, row),
+                        static_cast<uint16_t>(dk[i] >> 16));
+        }
+#pragma unroll
+        for (int i = 0; i < kHT / 2; ++i) {
+          st_shared_b16(sbase + kOffSP + hs_tile_off<kHG>(kHG + hb + 2 * i, row),
+                        static_cast<uint16_t>(pk[i]));
+          st_shared_b16(sbase + kOffSP + hs_tile_off<kHG>(kHG + hb + 2 * i + 1, row),
+                        static_cast<uint16_t>(pk[i] >> 16));
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(smem_u32(&m.ds_full));
-        // With a rope chunk, P goes into position 0 once the rope part of dQ
-        // has read the rope rows.
-        if constexpr (kRope) mbar_wait(smem_u32(&m.rope_done), gb & 1, fs, 9);
-#pragma unroll
-        for (int i = 0; i < kHT / 2; ++i) {
-          st_shared_b16(sbase + kOffP + hs_tile_off<kHG>(hb + 2 * i, row),
-                        static_cast<uint16_t>(pk[i]));
-          st_shared_b16(sbase + kOffP + hs_tile_off<kHG>(hb + 2 * i + 1, row),
-                        static_cast<uint16_t>(pk[i] >> 16));
-        }
-        fence_proxy_async_smem();
         named_bar_sync(1, kSoftmax);
         if (tid == 0) {
           // dS' and P rows of this head group -> the (token, block) scratch
@@ -575,36 +654,154 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
           const uint64_t pol = l2_evict_first();
           for (int half = 0; half < 2; ++half)
             for (int g2 = 0; g2 * 32 < nh; ++g2) {
-              tma_store_2d_hint(&tm_sp, half * 64, row0 + g2 * 32,
-                                sbase + kOffdS + half * kHChunk + g2 * 4096, pol);
-              tma_store_2d_hint(&tm_sp, half * 64, row0 + 32 * G32 + g2 * 32,
-                                sbase + kOffP + half * kHChunk + g2 * 4096, pol);
+              const uint32_t src = sbase + kOffSP + half * (2 * kHChunk) + g2 * 4096;
+              tma_store_2d_hint(&tm_sp, half * 64, row0 + g2 * 32, src, pol);
+              tma_store_2d_hint(&tm_sp, half * 64, row0 + 32 * G32 + g2 * 32, src + kHChunk, pol);
             }
           bulk_commit();
           bulk_wait_read();
-          if constexpr (kRope) mbar_arrive(smem_u32(&m.kv_free[0]));  // position 0 may take the next rope rows
         }
       }
-      // dQ^T -> dq (bf16), straight from registers: for each head, a warp
-      // writes 32 consecutive d of that head's row.
+      // ---------------------------------------------------------- epilogue
+      // The rounding remainders, summed over this warp's 32 rows: a butterfly
+      // reduce-scatter leaves lane L with head hb + (L mod kHT).
+      float esum_mine;
+      {
+        float ev[kHT];
+#pragma unroll
+        for (int i = 0; i < kHT / 2; ++i) {
+          ev[2 * i] = __low2float(eacc[i]);
+          ev[2 * i + 1] = __high2float(eacc[i]);
+        }
+#pragma unroll
+        for (int o = 16; o >= kHT; o >>= 1) {
+#pragma unroll
+          for (int i = 0; i < kHT; ++i) ev[i] += __shfl_xor_sync(0xffffffffu, ev[i], o);
+        }
+#pragma unroll
+        for (int o = kHT / 2; o > 0; o >>= 1) {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < o; ++i) {
+            const float keep = up ? ev[i + o] : ev[i];
+            const float send = up ? ev[i] : ev[i + o];
+            ev[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        esum_mine = ev[0];
+      }
+      // The out values of the dq correction, for this warp's 32 d rows of
+      // each V tile and its kHT heads, as 16-byte pieces (lane L: piece
+      // L + 32 k is head (L + 32 k) / 4, d columns 8 ((L + 32 k) % 4) ..),
+      // loaded while the last dQ MMAs run; redistributed through shared
+      // memory below.
+      const __nv_bfloat16* out_t = out + (static_cast<size_t>(t) * H + h0) * kDv;
+      constexpr int kPieces = kHT / 8;  // per lane per tile
+      uint4 opc[4][kPieces];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int k = 0; k < kPieces; ++k) {
+          const int pc = lane + 32 * k, hh = hb + pc / 4;
+          opc[j][k] = hh < nh ? __ldg(reinterpret_cast<const uint4*>(
+                                    out_t + static_cast<size_t>(hh) * kDv + j * 128 +
+                                    (warp & 3) * 32 + (pc & 3) * 8))
+                              : make_uint4(0, 0, 0, 0);
+        }
       mbar_wait(smem_u32(&m.dq_full), it & 1, fs, 10);
       tc_fence_after();
+      // The four row warps' remainder sums meet in the dS'/P tile (after the
+      // out slices below, 8 warps x kHT x 64 bytes).  The tile is free once
+      // thread 0 has seen the last block's scratch stores read it: its bulk
+      // wait precedes this barrier.
+      float* esum = reinterpret_cast<float*>(smem + kOffSP + 8 * kHT * 64);  // [4][kHG]
+      named_bar_sync(1, kSoftmax);
+      if (lane < kHT) esum[(warp & 3) * kHG + hb + lane] = esum_mine;
+      // sigma per head: the rope tile's filler rows (64..127), or rows 0..63
+      // of the separate sum tile without a rope chunk.
+      if ((warp & 3) == (kRope ? 2 : 0)) {
+        uint32_t v[kHT];
+        if constexpr (kHT == 32)
+          tmem_ld32_sync(tmem + lane_base + kColTail + hb, v);
+        else
+          tmem_ld16_sync(tmem + lane_base + kColTail + hb, v);
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < kHT; ++i) m.cd[hb + i].x = __uint_as_float(v[i]);
+        }
+      }
+      named_bar_sync(1, kSoftmax);
+      if (tid < kHG) {
+        float c = 0.f;
+        if (tid < nh) {
+          const size_t r = static_cast<size_t>(t) * H + h0 + tid;
+          const float sig = m.cd[tid].x + ((esum[tid] + esum[kHG + tid]) +
+                                           (esum[2 * kHG + tid] + esum[3 * kHG + tid]));
+          c = sig + scale * dsink_h;             // dsink_h = -p_sink * delta_a
+          cfix_g[r] = c;                         // = scale * (delta - delta_a)
+          const float eps = scale != 0.f ? c / scale : 0.f;
+          dsink_t[r] = dsink_h - (1.f - gate_h) * eps;  // p_sink = 1 - gate
+        }
+        m.cd[tid].y = c;
+      }
+      named_bar_sync(1, kSoftmax);
+      // dQ^T -> dq (bf16) straight from registers, with the delta correction:
+      // for each head, a warp writes 32 consecutive d of that head's row.
       __nv_bfloat16* dq_t = dq + (static_cast<size_t>(t) * H + h0) * kD;
-      for (int j = 0; j < kDT; ++j) {
+      // this warp's [kHT heads x 32 d] bf16 slice of out, 64 bytes per head
+      const uint32_t oslice = sbase + kOffSP + warp * (kHT * 64);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
         const int d = j * 128 + row;
+#pragma unroll
+        for (int k = 0; k < kPieces; ++k) {
+          const int pc = lane + 32 * k;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(oslice + pc * 16),
+                       "r"(opc[j][k].x), "r"(opc[j][k].y), "r"(opc[j][k].z), "r"(opc[j][k].w)
+                       : "memory");
+        }
+        __syncwarp();
+        float o[kHT];
+#pragma unroll
+        for (int i = 0; i < kHT; ++i) {
+          uint16_t b;
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(b) : "r"(oslice + i * 64 + lane * 2));
+          o[i] = __uint_as_float(static_cast<uint32_t>(b) << 16);
+        }
+        __syncwarp();  // the slice is rewritten for the next tile
         uint32_t v[kHT];
         if constexpr (kHT == 32)
           tmem_ld32_sync(tmem + lane_base + kColdQ + j * kHG + hb, v);
         else
           tmem_ld16_sync(tmem + lane_base + kColdQ + j * kHG + hb, v);
-        if (d < kD) {
+#pragma unroll
+        for (int i = 0; i < kHT; ++i) {
+          const int h = hb + i;
+          if (h < nh)
+            dq_t[static_cast<size_t>(h) * kD + d] =
+                __float2bfloat16_rn(fmaf(-m.cd[h].y, o[i], __uint_as_float(v[i])));
+        }
+      }
+      if constexpr (kRope) {
+        if ((warp & 3) < 2) {  // rows 0..63: d 512..575
+          const int d = 512 + row;
+          uint32_t v[kHT], w[kHT];
+          if constexpr (kHT == 32)
+            tmem_ld32x2_sync(tmem + lane_base + kColTail + hb, v,
+                             tmem + lane_base + kColTail + kHG + hb, w);
+          else
+            tmem_ld16x2_sync(tmem + lane_base + kColTail + hb, v,
+                             tmem + lane_base + kColTail + kHG + hb, w);
 #pragma unroll
           for (int i = 0; i < kHT; ++i) {
             const int h = hb + i;
-            if (h < nh) dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(__uint_as_float(v[i]));
+            if (h < nh)
+              dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(
+                  fmaf(-m.cd[h].y, __uint_as_float(w[i]), __uint_as_float(v[i])));
           }
         }
       }
+      named_bar_sync(1, kSoftmax);  // m.cd is rewritten at the next item's start
       ++it;
     }
   }
@@ -625,10 +822,13 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 // written by k_bwd_dq (MN-major).  With d on the TMEM lanes, each warp-level
 // atomic adds 128 contiguous bytes of one KV row, and there is one partial per
 // valid slot, however many head groups there are.
+// Before the GEMM of a block, the fixup warps apply the delta correction of
+// k_bwd_dq to the loaded tile: dS'' = dS' - c_h P per head row.
 namespace dkv {
 constexpr int kDrainWarps = 16;             // 4 per sub-partition, 32 slots each
-constexpr int kThreads = (kDrainWarps + 2) * 32;
-constexpr int kTmaWarp = kDrainWarps, kMmaWarp = kDrainWarps + 1;
+constexpr int kFixWarps = 4;                // the dS' correction of each loaded tile
+constexpr int kThreads = (kDrainWarps + 2 + kFixWarps) * 32;
+constexpr int kTmaWarp = kDrainWarps, kMmaWarp = kDrainWarps + 1, kFixWarp0 = kDrainWarps + 2;
 constexpr int kBTile = 64 * 4 * 128 * 2;    // up to 256 rows x 128 slots bf16 = 64 KB
 constexpr int kAStage = 4 * 128 * 128;      // Q and dO, 2 boxes each of up to 128 heads x 64 d
 constexpr int kOffB = 0;
@@ -641,7 +841,8 @@ constexpr int kOffMisc = kOffStage + 4 * kStageQ;
 constexpr uint32_t kTmemCols = 256;         // 2 accumulators of 128 columns
 
 struct Misc {
-  uint64_t b_full, b_empty, a_full[2], a_empty[2], d_full[2], d_empty[2], mma_done;
+  uint64_t b_full, b_fixed, b_empty, a_full[2], a_empty[2], d_full[2], d_empty[2], mma_done;
+  float c[128];       // the token's per-head correction c_h (0 past H)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -656,7 +857,8 @@ template <bool kDet, int kD>
 __global__ void __launch_bounds__(dkv::kThreads, 1)
 k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUtensorMap tm_doa,
           const __grid_constant__ CUtensorMap tm_spb, const int32_t* __restrict__ idxc,
-          const int32_t* __restrict__ count, void* __restrict__ dkv_acc, int T, int H, int W,
+          const int32_t* __restrict__ count, const float* __restrict__ cfix,
+          void* __restrict__ dkv_acc, unsigned int* __restrict__ row_max, int T, int H, int W,
           int G, int box_heads, int nbmax) {
   using dkv::kDrainWarps;
   using dkv::kTmaWarp;
@@ -684,6 +886,7 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
 
   if (tid == 0) {
     mbar_init(smem_u32(&m.b_full), 1);
+    mbar_init(smem_u32(&m.b_fixed), dkv::kFixWarps * 32);
     mbar_init(smem_u32(&m.b_empty), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&m.a_full[i]), 1);
@@ -759,7 +962,7 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         if (Kt == 0) continue;
         const int nblk = (Kt + kBlk - 1) / kBlk;
         for (int b = 0; b < nblk; ++b, ++gb) {
-          mbar_wait(smem_u32(&m.b_full), gb & 1, fs, 22);
+          mbar_wait(smem_u32(&m.b_fixed), gb & 1, fs, 22);
           for (int n = 0; n < kNT; ++n) {
             const int u = gb * kNT + n, st = u & 1, use = u >> 1;
             mbar_wait(smem_u32(&m.a_full[st]), use & 1, fs, 23);
@@ -793,6 +996,62 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
       }
     }
     __syncwarp();
+  } else if (warp >= dkv::kFixWarp0) {
+    // ------------------------------------------------------------ dS' fixup
+    // dS'' = dS' - c_h P on every 16-byte piece of the loaded tile: row h of
+    // the dS' rows and row HP + h of the P rows share their swizzle phase, so
+    // the same piece index holds the same slots in both.
+    const int ftid = tid - dkv::kFixWarp0 * 32;
+    constexpr int kFixThreads = dkv::kFixWarps * 32;
+    int gb = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+      const int Kt = count[t];
+      if (Kt == 0) continue;
+      const int nblk = (Kt + kBlk - 1) / kBlk;
+      named_bar_sync(6, kFixThreads);  // the previous token's pieces are all done
+      for (int h = ftid; h < HP; h += kFixThreads)
+        m.c[h] = h < H ? cfix[static_cast<size_t>(t) * H + h] : 0.f;
+      named_bar_sync(6, kFixThreads);
+      for (int b = 0; b < nblk; ++b, ++gb) {
+        mbar_wait(smem_u32(&m.b_full), gb & 1, fs, 26);
+        // 16 HP pieces (a multiple of 4 x 128): four independent pieces per
+        // round, loads first, so that their latencies overlap
+        for (int p0 = ftid; p0 < 16 * HP; p0 += 4 * kFixThreads) {
+          uint32_t a[4], dw[4][4], pw[4][4];
+          float c[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int pce = p0 + u * kFixThreads;
+            const int box = pce / (8 * HP), rem = pce - box * 8 * HP;
+            c[u] = m.c[rem >> 3];
+            a[u] = sbase + kOffB + box * b_half + rem * 16;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(dw[u][0]), "=r"(dw[u][1]), "=r"(dw[u][2]), "=r"(dw[u][3])
+                         : "r"(a[u]));
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(pw[u][0]), "=r"(pw[u][1]), "=r"(pw[u][2]), "=r"(pw[u][3])
+                         : "r"(a[u] + static_cast<uint32_t>(HP) * 128u));
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (c[u] == 0.f) continue;  // padded heads, or nothing to correct
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 d2 =
+                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[u][k]));
+              const float2 p2 =
+                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[u][k]));
+              dw[u][k] = pack_bf16x2(fmaf(-c[u], p2.x, d2.x), fmaf(-c[u], p2.y, d2.y));
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a[u]), "r"(dw[u][0]),
+                         "r"(dw[u][1]), "r"(dw[u][2]), "r"(dw[u][3])
+                         : "memory");
+          }
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> the UMMA reads
+        mbar_arrive(smem_u32(&m.b_fixed));
+      }
+    }
   } else {
     // ------------------------------------------------------------ drain
     // Warp w reads TMEM lanes 32 (w % 4) .. +31 (d rows of the chunk) and
@@ -827,7 +1086,14 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
 #pragma unroll
               for (int s = 0; s < 32; ++s) {
                 const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
-                if (s < nvalid) red_add_fixed32(dst + o, __uint_as_float(v[s]), keep);
+                if (s < nvalid) {
+                  const float f = __uint_as_float(v[s]);
+                  red_add_fixed32(dst + o, f, keep);
+                  // largest |v| added to the row (non-negative floats order
+                  // like their bit patterns; NaN counts as the largest)
+                  const uint32_t mx = redux_max_u32(__float_as_uint(fabsf(f)));
+                  if (lane == 0) atomicMax(row_max + o / kD, mx);
+                }
               }
             }
           }
@@ -884,11 +1150,22 @@ k_dkv_cast(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dkv, long 
   reinterpret_cast<uint4*>(dkv)[i] = o;
 }
 
-// The fixed-point accumulator (int64, units of 2^-32) -> bf16 dkv.
+// The fixed-point accumulator (int64, units of 2^-32) -> bf16 dkv.  Every
+// element of row r received row_refs[r] adds, each at most row_max[r] in
+// magnitude, so its sum stayed inside the accumulator's +-2^31 when their
+// product is below 2^31; otherwise the row may have wrapped, and the error
+// word says so (DSA_ERR_RANGE).
 __global__ void __launch_bounds__(256)
-k_dkv_cast_fixed(const long long* __restrict__ acc, __nv_bfloat16* __restrict__ dkv, long long n8) {
+k_dkv_cast_fixed(const long long* __restrict__ acc, __nv_bfloat16* __restrict__ dkv, long long n8,
+                 const unsigned int* __restrict__ row_refs,
+                 const unsigned int* __restrict__ row_max, int D) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n8) return;
+  if ((8 * i) % D == 0) {  // first piece of a row
+    const long long r = 8 * i / D;
+    const float bound = static_cast<float>(row_refs[r]) * __uint_as_float(row_max[r]);
+    if (!(bound < 2147483648.0f)) atomicCAS(&g_err_bwd, 0u, kErrDetRange);
+  }
   float f[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) f[j] = fixed32_to_float(acc[8 * i + j]);
@@ -916,13 +1193,41 @@ k_dsink(const float* __restrict__ dsink_t, float* __restrict__ dsink, int T, int
   if (threadIdx.x == 0) dsink[h] = red[0];
 }
 
+// ------------------------------------------------------------------ wait self-test
+
+// Two waits on barriers that nothing completes: thread 0 with a short limit,
+// thread 32 with the ordinary one.  The first gives up, records a timeout in
+// the error word and raises the abort flag, which ends the second wait at its
+// next check; then the kernel returns and the context stays usable.
+__global__ void __launch_bounds__(64) k_wait_selftest(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar[0]), 1);
+    mbar_init(smem_u32(&bar[1]), 1);
+    abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const FailState fs{&g_err_bwd, &abort_flag};
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar[0]), 0, fs, 0x30, limit_ns);
+  if (threadIdx.x == 32) mbar_wait(smem_u32(&bar[1]), 0, fs, 0x31);
+  __syncthreads();
+}
+
 }  // namespace
 
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
+  k_wait_selftest<<<1, 64, 0, s>>>(limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_compact(const Problem& p, const int32_t* idx, const int32_t* len,
-                           int32_t* idx_out, int32_t* count_out, cudaStream_t s) {
+                           int32_t* idx_out, int32_t* count_out, cudaStream_t s,
+                           unsigned int* row_refs) {
   if (p.T == 0) return cudaSuccess;
   k_compact<<<p.T, kCompactThreads, 0, s>>>(idx, len, idx_out, count_out, p.W, p.S_kv, p.cu_q,
-                                            p.cu_kv, p.B);
+                                            p.cu_kv, p.B, row_refs);
   return cudaGetLastError();
 }
 
@@ -946,7 +1251,7 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
       e = cudaFuncSetAttribute(k_bwd_dq<512, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                DqLayout<512, 32>::kSmemBytes);
     void (*dkv_kernels[])(CUtensorMap, CUtensorMap, CUtensorMap, const int32_t*, const int32_t*,
-                          void*, int, int, int, int, int, int) = {
+                          const float*, void*, unsigned int*, int, int, int, int, int, int) = {
         k_bwd_dkv<false, 576>, k_bwd_dkv<true, 576>, k_bwd_dkv<false, 512>, k_bwd_dkv<true, 512>};
     for (auto k : dkv_kernels)
       if (e == cudaSuccess)
@@ -957,19 +1262,23 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
   const BwdWorkspace L = bwd_workspace_layout(p);
   uint8_t* base = static_cast<uint8_t*>(ws);
   void* acc = base + L.dkv_acc;
+  unsigned int* row_refs =
+      p.deterministic ? reinterpret_cast<unsigned int*>(base + L.det_count) : nullptr;
+  unsigned int* row_max =
+      p.deterministic ? reinterpret_cast<unsigned int*>(base + L.det_max) : nullptr;
   int32_t* idxc = reinterpret_cast<int32_t*>(base + L.idxc);
   int32_t* count = reinterpret_cast<int32_t*>(base + L.count);
   float* lse2 = reinterpret_cast<float*>(base + L.lse2);
   float* gate = reinterpret_cast<float*>(base + L.gate);
   float* delta = reinterpret_cast<float*>(base + L.delta);
   float* dsink_t = reinterpret_cast<float*>(base + L.dsink_t);
-  const size_t acc_bytes = static_cast<size_t>(p.S_kv) * p.d_qk * (p.deterministic ? 8 : 4);
+  float* cfix = reinterpret_cast<float*>(base + L.cfix);
   cudaError_t e = cudaSuccess;
   if (stages & kBwdPre) {
-    e = cudaMemsetAsync(acc, 0, acc_bytes, s);
+    e = cudaMemsetAsync(acc, 0, L.zero_bytes - L.dkv_acc, s);
     if (e != cudaSuccess) return e;
     if (p.T > 0) {
-      e = launch_compact(p, idx, len, idxc, count, s);
+      e = launch_compact(p, idx, len, idxc, count, s, row_refs);
       if (e != cudaSuccess) return e;
       const long long rows = static_cast<long long>(p.T) * p.H;
       k_bwd_pre<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(
@@ -1004,8 +1313,8 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
     kern<<<grid, kThreads, smem, s>>>(
         tm_q, tm_do, tm_sp_st, tm_kv, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2,
-        gate,
-        delta, static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, G32, box_heads, nbmax);
+        gate, delta, static_cast<const __nv_bfloat16*>(out), dsink_t, cfix,
+        static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, G32, box_heads, nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1027,7 +1336,8 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     // persistent CTAs that prefetch the next token.
     const int grid = p.deterministic && p.T > sm_count() ? sm_count() : p.T;
     kern<<<grid, dkv::kThreads, dkv::kSmemBytes, s>>>(
-        tm_qa, tm_doa, tm_sp_ld, idxc, count, acc, p.T, p.H, p.W, G, box_all, nbmax);
+        tm_qa, tm_doa, tm_sp_ld, idxc, count, cfix, acc, row_max, p.T, p.H, p.W, G, box_all,
+        nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1035,7 +1345,8 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     const long long n8 = static_cast<long long>(p.S_kv) * p.d_qk / 8;
     if (p.deterministic)
       k_dkv_cast_fixed<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
-          static_cast<const long long*>(acc), static_cast<__nv_bfloat16*>(dkv), n8);
+          static_cast<const long long*>(acc), static_cast<__nv_bfloat16*>(dkv), n8, row_refs,
+          row_max, p.d_qk);
     else
       k_dkv_cast<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(
           static_cast<const float*>(acc), static_cast<__nv_bfloat16*>(dkv), n8);

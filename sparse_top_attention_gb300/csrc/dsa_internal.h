@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+#include "../../include/dsa.h"
+
 namespace dsa {
 
 struct Problem {
@@ -24,12 +26,16 @@ struct Problem {
 // Byte offsets inside the backward workspace (256-byte aligned pieces).
 struct BwdWorkspace {
   size_t dkv_acc;   // fp32 [S_kv, 576], or int64 [S_kv, 576] in 2^-32 units when deterministic
+  size_t det_count; // u32 [S_kv]     deterministic only: valid slots naming each KV row
+  size_t det_max;   // u32 [S_kv]     deterministic only: largest |add| per row (fp32 bits)
+  size_t zero_bytes;  // end of the region zeroed before the backward (from dkv_acc = 0)
   size_t idxc;      // int32 [T, W]   compacted rows
   size_t count;     // int32 [T]
   size_t lse2;      // fp32 [T, H]    lse * log2(e), 0 for empty rows
   size_t gate;      // fp32 [T, H]    sigma(lse - sink), 0 for empty rows
   size_t delta;     // fp32 [T, H]    rowsum(dout * out)
-  size_t dsink_t;   // fp32 [T, H]    -p_sink * delta
+  size_t dsink_t;   // fp32 [T, H]    -p_sink * delta (the exact delta once the main stage ran)
+  size_t cfix;      // fp32 [T, H]    scale * (exact delta - delta from out), from the main stage
   size_t sp;        // bf16 [T, nbmax, 64G, 128]: per (token, 128-slot block) the
                     // dS' rows (32G heads) then the P rows (32G heads), slots
                     // contiguous; G = ceil(H / 32), nbmax = ceil(W / 128)
@@ -61,13 +67,17 @@ inline int sm_count() {
 inline int bwd_groups(int H) { return (H + 31) / 32; }
 inline int bwd_nbmax(int W) { return (W + 127) / 128; }
 BwdWorkspace bwd_workspace_layout(const Problem& p);
+// Validates the problem as every entry point does, then gives the backward's
+// workspace size; the status is that of the failed check.
+dsa_status_t bwd_workspace_checked(const dsa_problem_t* problem, size_t* bytes);
 
 cudaError_t launch_fwd(const Problem& p, const void* q, const void* kv, const int32_t* idx,
                        const int32_t* len, const float* sink, void* out, float* lse,
                        cudaStream_t s);
 
 cudaError_t launch_compact(const Problem& p, const int32_t* idx, const int32_t* len,
-                           int32_t* idx_out, int32_t* count_out, cudaStream_t s);
+                           int32_t* idx_out, int32_t* count_out, cudaStream_t s,
+                           unsigned int* row_refs = nullptr);
 
 // Backward stages; stage mask bit 0 = preprocess, 1 = main, 2 = finalize.
 enum : int { kBwdPre = 1, kBwdMain = 2, kBwdFinal = 4, kBwdAll = 7 };
@@ -76,7 +86,14 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
                        const void* dout, void* dq, void* dkv, float* dsink, void* ws,
                        cudaStream_t s, int stages);
 
+// One small kernel whose barrier waits run out after limit_ns (the bounded-
+// wait self-test behind dsa_wait_selftest).
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
+
 // Device error words (one per translation unit): read-and-clear after a sync.
+// 0x1xx are wait timeouts (the low byte says where); kErrDetRange is the
+// deterministic accumulator's range check.
+constexpr unsigned int kErrDetRange = 0x4FFu;
 unsigned int fwd_take_error();
 unsigned int bwd_take_error();
 

@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/dsa.h"
+#include "dsa_internal.h"
 
 namespace {
 
@@ -55,8 +56,11 @@ extern "C" dsa_status_t dsa_bwd_no_alloc(const dsa_problem_t* problem, const voi
                                          const int32_t* topk_length, const float* sink,
                                          const void* out, const float* lse, const void* dout,
                                          void* dq, void* dkv, float* dsink, void* stream) {
-  const size_t need = dsa_bwd_workspace_bytes(problem);
-  if (need == 0) return DSA_ERR_INVALID_ARG;
+  // The problem is checked exactly as dsa_bwd checks it (same status codes);
+  // only then is its workspace compared with the array.
+  size_t need = 0;
+  const dsa_status_t chk = dsa::bwd_workspace_checked(problem, &need);
+  if (chk != DSA_OK) return chk;
   if (need > kNoAllocBytes) return DSA_ERR_WORKSPACE;
   void* ws = nullptr;
   const dsa_status_t st = workspace_address(&ws);

@@ -94,20 +94,27 @@ struct FailState {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const FailState& fs,
-                                          uint32_t where) {
+                                          uint32_t where, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*fs.abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *fs.abort_flag = 1;
         atomicCAS(fs.err_word, 0u, 0x100u | where);
         return false;
       }
     }
   }
+}
+
+// Largest of the 32 lanes' values (every lane of the warp must take part).
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
 }
 
 // ----------------------------------------------------------------- cp.async
@@ -206,6 +213,12 @@ __device__ __forceinline__ void bulk_store_hint(void* gdst, uint32_t ssrc, uint3
                    gdst),
                "r"(ssrc), "r"(bytes), "l"(pol)
                : "memory");
+}
+
+// Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2
+// ahead of use; no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Fixed-point accumulation in units of 2^-32 (two's complement in a u64):

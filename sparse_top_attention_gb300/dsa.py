@@ -23,13 +23,14 @@ LIB_PATH = os.path.join(_HERE, "_build", "libdsa.so")
 
 STATUS = {
     0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_ALIGNMENT",
-    4: "DSA_ERR_WORKSPACE", 5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_TIMEOUT",
+    4: "DSA_ERR_WORKSPACE", 5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_TIMEOUT", 7: "DSA_ERR_RANGE",
 }
 
 # Every symbol that include/dsa.h declares.
 EXPORTS = ("dsa_fwd", "dsa_bwd_workspace_bytes", "dsa_bwd", "dsa_bwd_preprocess", "dsa_bwd_main",
            "dsa_bwd_finalize", "dsa_bwd_no_alloc", "dsa_fwd_varlen", "dsa_bwd_varlen",
-           "dsa_topk_compact", "dsa_device_status", "dsa_status_string", "dsa_version")
+           "dsa_topk_compact", "dsa_device_status", "dsa_wait_selftest", "dsa_status_string",
+           "dsa_version")
 BWD_STAGES = ("dsa_bwd_preprocess", "dsa_bwd_main", "dsa_bwd_finalize")
 FLAG_DELTA_RESIDUAL = 1
 FLAG_DETERMINISTIC = 2
@@ -89,6 +90,8 @@ def library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.dsa_topk_compact.restype = ctypes.c_int
     lib.dsa_device_status.argtypes = [vp]
     lib.dsa_device_status.restype = ctypes.c_int
+    lib.dsa_wait_selftest.argtypes = [ctypes.c_uint32, vp]
+    lib.dsa_wait_selftest.restype = ctypes.c_int
     lib.dsa_status_string.argtypes = [ctypes.c_int]
     lib.dsa_status_string.restype = ctypes.c_char_p
     lib.dsa_version.argtypes = []
@@ -290,6 +293,13 @@ def topk_compact(topk_idxs, topk_length, S_kv, stream=None):
                                       _ptr(idx_out), _ptr(count), _stream(stream)),
            "dsa_topk_compact")
     return idx_out, count
+
+
+def wait_selftest(limit_us: int, stream=None) -> None:
+    """Queue the bounded-wait self-test (dsa_wait_selftest): a kernel whose
+    barrier waits run out after ``limit_us`` microseconds.  The next
+    ``device_status`` returns DSA_ERR_DEVICE_TIMEOUT."""
+    _check(library().dsa_wait_selftest(int(limit_us), _stream(stream)), "dsa_wait_selftest")
 
 
 def device_status(stream=None) -> int:

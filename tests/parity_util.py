@@ -57,8 +57,7 @@ def check_fwd(out, lse, ref, counts, rows=None):
     return errs
 
 
-def check_bwd(dq, dkv, dsink, g, counts, rows=None, check_dkv=True, check_dsink=True,
-              dkv_tol=REL_TOL):
+def check_bwd(dq, dkv, dsink, g, counts, rows=None, check_dkv=True, check_dsink=True):
     assert_finite(dq=dq, dkv=dkv, dsink=dsink)
     dq_np = np64(dq)
     sel = np.arange(dq_np.shape[0]) if rows is None else np.asarray(rows)
@@ -74,7 +73,7 @@ def check_bwd(dq, dkv, dsink, g, counts, rows=None, check_dkv=True, check_dsink=
     if check_dsink and dsink is not None:
         errs["dsink"] = rel_frob(dsink, g["dsink"])
     for k, v in errs.items():
-        assert v <= (dkv_tol if k == "dkv" else REL_TOL), errs
+        assert v <= REL_TOL, errs
     return errs
 
 
@@ -82,3 +81,26 @@ def per_head_rel(a, ref):
     a, ref = np64(a), np64(ref)
     H = a.shape[1]
     return [rel_frob(a[:, h], ref[:, h]) for h in range(H)]
+
+
+def check_per_head(a, ref, what):
+    """Every head on its own within the bar (a head whose reference is all
+    zero, e.g. under a positive saturating sink, must be exactly zero), so
+    that one wrong sink-stress head cannot hide under the others' norm."""
+    errs = per_head_rel(a, ref)
+    bad = {h: e for h, e in enumerate(errs) if not e <= REL_TOL}
+    assert not bad, f"{what}: heads over the bar {bad}"
+    return errs
+
+
+def check_per_head_dsink(dsink, ref):
+    """d_sink head by head: exact zeros where the reference is zero (no sink
+    share, or a sink that takes the whole denominator with out = 0), else a
+    relative error within the bar."""
+    a, r = np64(dsink), np64(ref)
+    floor = 1e-3 * float(np.abs(r).max()) if r.size else 0.0
+    for h in range(r.shape[0]):
+        if r[h] == 0:
+            assert a[h] == 0, (h, a[h])
+        else:
+            assert abs(a[h] - r[h]) <= REL_TOL * max(abs(r[h]), floor), (h, a[h], r[h])

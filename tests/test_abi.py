@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.dsa_version() == 100
-    for code in range(7):
+    for code in range(8):
         assert len(lib.dsa_status_string(code)) > 0
 
 
@@ -49,9 +49,10 @@ def test_workspace_size_is_pure_host(lib):
     assert n >= 5120 * 576 * 4 + 4096 * 640 * 4 + 4 * 4096 * 128 * 4
     assert n % 256 == 0
     assert lib.dsa_bwd_workspace_bytes(ctypes.byref(P(H=0))) == 0
-    # DSA_FLAG_DETERMINISTIC keeps dkv as int64: 4 more bytes per accumulator element
+    # DSA_FLAG_DETERMINISTIC keeps dkv as int64 (4 more bytes per accumulator
+    # element) plus two u32 per KV row for its range check
     nd = lib.dsa_bwd_workspace_bytes(ctypes.byref(P(T=4096, H=128, S_kv=5120, W=640, flags=2)))
-    assert nd - n == 5120 * 576 * 4
+    assert nd - n == 5120 * 576 * 4 + 2 * 5120 * 4
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -87,6 +88,22 @@ def test_backward_argument_checks(lib):
     # workspace misaligned
     w = ctypes.c_void_p((1 << 20) + 16)
     assert lib.dsa_bwd(ctypes.byref(p), a, a, a, None, None, a, a, a, a, a, None, w, n, None) == 3
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=129), 2), (dict(d_qk=640), 2), (dict(S_kv=3728271), 2), (dict(H=0), 1),
+    (dict(flags=8), 1),
+])
+def test_no_alloc_passes_the_check_status_through(lib, kw, code):
+    """dsa_bwd_no_alloc validates a problem as dsa_bwd does and returns the
+    same status (not a generic one), before it touches the device."""
+    p = P(**kw)
+    a = ctypes.c_void_p(1 << 20)
+    n = ctypes.c_size_t(1 << 30)
+    assert lib.dsa_bwd(ctypes.byref(p), a, a, a, None, None, a, a, a, a, a, None, a, n,
+                       None) == code
+    assert lib.dsa_bwd_no_alloc(ctypes.byref(p), a, a, a, None, None, a, a, a, a, a, None,
+                                None) == code
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -10,7 +10,7 @@ from oracle import dsa_oracle as O
 from sparse_top_attention_gb300 import dsa
 from sparse_top_attention_gb300 import workloads as WL
 from tests.parity_util import REL_TOL, check_bwd, check_fwd, np64, rel_frob
-from tests.test_gpu_parity import (_lib, _sample_tokens, counts_of, oracle_all,  # noqa: F401
+from tests.test_gpu_parity import (_lib, _sample_tokens, counts_of, oracle_exact,  # noqa: F401
                                    run)
 from tests.test_gpu_varlen import oracle_varlen, run_varlen
 
@@ -32,7 +32,7 @@ def test_d512_parity_small(name, kw):
     w = d512(name, kw)
     assert w.q.shape[2] == 512 and w.kv.shape[1] == 512
     out, lse, dq, dkv, dsink = run(w)
-    ref, g = oracle_all(w)
+    ref, g = oracle_exact(w)
     counts = counts_of(w)
     check_fwd(out, lse, ref, counts)
     check_bwd(dq, dkv, dsink, g, counts)
@@ -57,7 +57,7 @@ def test_d512_varlen():
     out, lse, dq, dkv, dsink = run_varlen(w)
     ref, g = oracle_varlen(w)
     check_fwd(out, lse, ref, ref["count"])
-    check_bwd(dq, dkv, dsink, g, ref["count"], dkv_tol=REL_TOL)
+    check_bwd(dq, dkv, dsink, g, ref["count"])
 
 
 def test_d512_full_size_sampled():
@@ -69,10 +69,10 @@ def test_d512_full_size_sampled():
     out, lse, dq, dkv, dsink = run(w)
     counts = counts_of(w)
     toks = _sample_tokens(w.T, rng)
-    ref, g = oracle_all(w, tokens=toks)
+    ref, g = oracle_exact(w, tokens=toks)
     check_fwd(out, lse, ref, counts, rows=toks)
     check_bwd(dq, None, None, g, counts, rows=toks, check_dkv=False, check_dsink=False)
     rows = [5, w.T // 3, w.S_kv - 1, w.S_kv - 2]
     rtoks = O.tokens_referencing(w.topk_idxs, w.topk_length, w.S_kv, rows)
-    _, gr = oracle_all(w, tokens=rtoks)
+    _, gr = oracle_exact(w, tokens=rtoks)
     assert rel_frob(np64(dkv)[rows], gr["dkv"][rows]) <= REL_TOL

@@ -8,7 +8,7 @@ from oracle import dsa_oracle as O
 from sparse_top_attention_gb300 import dsa
 from sparse_top_attention_gb300 import workloads as WL
 from tests.parity_util import REL_TOL, check_bwd, check_fwd
-from tests.test_gpu_parity import DEV, _lib, bf16_stored  # noqa: F401
+from tests.test_gpu_parity import DEV, _lib  # noqa: F401
 from tests.test_oracle_varlen import _with_out_of_sequence_indices
 
 pytestmark = pytest.mark.gpu
@@ -37,7 +37,7 @@ def oracle_varlen(w):
     ref = O.forward_varlen(w.q, w.kv, w.topk_idxs, w.topk_length, w.sink, w.scale,
                            w.cu_seqlens_q, w.cu_seqlens_kv)
     g = O.backward_varlen(w.q, w.kv, w.topk_idxs, w.topk_length, w.sink, w.scale, w.dout,
-                          w.cu_seqlens_q, w.cu_seqlens_kv, out=bf16_stored(ref["out"]))
+                          w.cu_seqlens_q, w.cu_seqlens_kv)
     return ref, g
 
 
@@ -48,7 +48,7 @@ def test_varlen_parity(lengths, H, topk, compact, seed):
     out, lse, dq, dkv, dsink = run_varlen(w)
     ref, g = oracle_varlen(w)
     check_fwd(out, lse, ref, ref["count"])
-    check_bwd(dq, dkv, dsink, g, ref["count"], dkv_tol=REL_TOL)
+    check_bwd(dq, dkv, dsink, g, ref["count"])
 
 
 def test_varlen_sequence_without_kv_rows():
@@ -62,5 +62,5 @@ def test_varlen_sequence_without_kv_rows():
     ref, g = oracle_varlen(w)
     assert (ref["count"][:90] == 0).all()
     check_fwd(out, lse, ref, ref["count"])
-    check_bwd(dq, dkv, dsink, g, ref["count"], dkv_tol=REL_TOL)
+    check_bwd(dq, dkv, dsink, g, ref["count"])
     np.testing.assert_array_equal(dq[:90].float().cpu().numpy(), 0.0)
