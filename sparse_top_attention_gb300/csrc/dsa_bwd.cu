@@ -599,32 +599,31 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         mbar_wait(smem_u32(&m.s_full), gb & 1, fs, 7);
         tc_fence_after();
         const bool valid = b * kBlk + row < Kt;
-        uint32_t rs[kHT], rd[kHT];
-        if constexpr (kHT == 32)
-          tmem_ld32x2_sync(tmem + lane_base + kColS + hb, rs, tmem + lane_base + kColdP + hb, rd);
-        else
-          tmem_ld16x2_sync(tmem + lane_base + kColS + hb, rs, tmem + lane_base + kColdP + hb, rd);
-        float dsv[kHT];
         uint32_t pk[kHT / 2];  // P as bf16 pairs (heads hb + 2i, hb + 2i + 1)
-        const float4* cd4 = reinterpret_cast<const float4*>(m.cd + hb);
-#pragma unroll
-        for (int i = 0; i < kHT; i += 2) {
-          const float4 c = cd4[i / 2];  // heads hb + i, hb + i + 1
-          // Live columns satisfy s - lse <= 0, so exp2 never overflows here;
-          // rows past the valid count hold zero KV (finite dP) and get P = 0.
-          const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(rs[i]), sl2, c.x)) : 0.f;
-          const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(rs[i + 1]), sl2, c.z)) : 0.f;
-          dsv[i] = p0 * (__uint_as_float(rd[i]) - c.y) * scale;
-          dsv[i + 1] = p1 * (__uint_as_float(rd[i + 1]) - c.w) * scale;
-          pk[i / 2] = pack_bf16x2(p0, p1);
-        }
         uint32_t dk[kHT / 2];  // dS' as bf16 pairs
+        const float4* cd4 = reinterpret_cast<const float4*>(m.cd + hb);
+        // 16 heads at a time, so that only 32 loaded TMEM values are live
 #pragma unroll
-        for (int i = 0; i < kHT; i += 2) {
-          dk[i / 2] = pack_bf16x2(dsv[i], dsv[i + 1]);
-          const float r0 = dsv[i] - __uint_as_float(dk[i / 2] << 16);
-          const float r1 = dsv[i + 1] - __uint_as_float(dk[i / 2] & 0xFFFF0000u);
-          eacc[i / 2] = __hadd2(eacc[i / 2], __floats2bfloat162_rn(r0, r1));
+        for (int hh = 0; hh < kHT; hh += 16) {
+          uint32_t rs[16], rd[16];
+          tmem_ld16x2_sync(tmem + lane_base + kColS + hb + hh, rs,
+                           tmem + lane_base + kColdP + hb + hh, rd);
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const float4 c = cd4[(hh + i) / 2];  // heads hb + hh + i, + 1
+            // Live columns satisfy s - lse <= 0, so exp2 never overflows here;
+            // rows past the valid count hold zero KV (finite dP) and get P = 0.
+            const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(rs[i]), sl2, c.x)) : 0.f;
+            const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(rs[i + 1]), sl2, c.z)) : 0.f;
+            const float ds0 = p0 * (__uint_as_float(rd[i]) - c.y) * scale;
+            const float ds1 = p1 * (__uint_as_float(rd[i + 1]) - c.w) * scale;
+            const int q = (hh + i) / 2;
+            pk[q] = pack_bf16x2(p0, p1);
+            dk[q] = pack_bf16x2(ds0, ds1);
+            const float r0 = ds0 - __uint_as_float(dk[q] << 16);
+            const float r1 = ds1 - __uint_as_float(dk[q] & 0xFFFF0000u);
+            eacc[q] = __hadd2(eacc[q], __floats2bfloat162_rn(r0, r1));
+          }
         }
         if (gb > 0) mbar_wait(smem_u32(&m.dsp_free), (gb - 1) & 1, fs, 8);
         // thread 0 finished reading the previous block's tiles out (bulk wait below)
@@ -693,21 +692,23 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       // The out values of the dq correction, for this warp's 32 d rows of
       // each V tile and its kHT heads, as 16-byte pieces (lane L: piece
       // L + 32 k is head (L + 32 k) / 4, d columns 8 ((L + 32 k) % 4) ..),
-      // loaded while the last dQ MMAs run; redistributed through shared
-      // memory below.
+      // redistributed through shared memory below.  Two tiles in flight at
+      // a time (the first two while the last dQ MMAs run).
       const __nv_bfloat16* out_t = out + (static_cast<size_t>(t) * H + h0) * kDv;
       constexpr int kPieces = kHT / 8;  // per lane per tile
-      uint4 opc[4][kPieces];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
+      auto load_out = [&](int j, uint4 (&dst)[kPieces]) {
 #pragma unroll
         for (int k = 0; k < kPieces; ++k) {
           const int pc = lane + 32 * k, hh = hb + pc / 4;
-          opc[j][k] = hh < nh ? __ldg(reinterpret_cast<const uint4*>(
-                                    out_t + static_cast<size_t>(hh) * kDv + j * 128 +
-                                    (warp & 3) * 32 + (pc & 3) * 8))
-                              : make_uint4(0, 0, 0, 0);
+          dst[k] = hh < nh ? __ldg(reinterpret_cast<const uint4*>(
+                                 out_t + static_cast<size_t>(hh) * kDv + j * 128 +
+                                 (warp & 3) * 32 + (pc & 3) * 8))
+                           : make_uint4(0, 0, 0, 0);
         }
+      };
+      uint4 opc[2][kPieces];
+      load_out(0, opc[0]);
+      load_out(1, opc[1]);
       mbar_wait(smem_u32(&m.dq_full), it & 1, fs, 10);
       tc_fence_after();
       // The four row warps' remainder sums meet in the dS'/P tile (after the
@@ -756,10 +757,12 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 #pragma unroll
         for (int k = 0; k < kPieces; ++k) {
           const int pc = lane + 32 * k;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(oslice + pc * 16),
-                       "r"(opc[j][k].x), "r"(opc[j][k].y), "r"(opc[j][k].z), "r"(opc[j][k].w)
+          const uint4 x = opc[j & 1][k];
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(oslice + pc * 16), "r"(x.x),
+                       "r"(x.y), "r"(x.z), "r"(x.w)
                        : "memory");
         }
+        if (j < 2) load_out(j + 2, opc[j & 1]);
         __syncwarp();
         float o[kHT];
 #pragma unroll
@@ -785,19 +788,18 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       if constexpr (kRope) {
         if ((warp & 3) < 2) {  // rows 0..63: d 512..575
           const int d = 512 + row;
-          uint32_t v[kHT], w[kHT];
-          if constexpr (kHT == 32)
-            tmem_ld32x2_sync(tmem + lane_base + kColTail + hb, v,
-                             tmem + lane_base + kColTail + kHG + hb, w);
-          else
-            tmem_ld16x2_sync(tmem + lane_base + kColTail + hb, v,
-                             tmem + lane_base + kColTail + kHG + hb, w);
 #pragma unroll
-          for (int i = 0; i < kHT; ++i) {
-            const int h = hb + i;
-            if (h < nh)
-              dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(
-                  fmaf(-m.cd[h].y, __uint_as_float(w[i]), __uint_as_float(v[i])));
+          for (int hh = 0; hh < kHT; hh += 16) {
+            uint32_t v[16], w[16];
+            tmem_ld16x2_sync(tmem + lane_base + kColTail + hb + hh, v,
+                             tmem + lane_base + kColTail + kHG + hb + hh, w);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int h = hb + hh + i;
+              if (h < nh)
+                dq_t[static_cast<size_t>(h) * kD + d] = __float2bfloat16_rn(
+                    fmaf(-m.cd[h].y, __uint_as_float(w[i]), __uint_as_float(v[i])));
+            }
           }
         }
       }
@@ -826,7 +828,7 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 // k_bwd_dq to the loaded tile: dS'' = dS' - c_h P per head row.
 namespace dkv {
 constexpr int kDrainWarps = 16;             // 4 per sub-partition, 32 slots each
-constexpr int kFixWarps = 4;                // the dS' correction of each loaded tile
+constexpr int kFixWarps = 8;                // the dS' correction of each loaded tile
 constexpr int kThreads = (kDrainWarps + 2 + kFixWarps) * 32;
 constexpr int kTmaWarp = kDrainWarps, kMmaWarp = kDrainWarps + 1, kFixWarp0 = kDrainWarps + 2;
 constexpr int kBTile = 64 * 4 * 128 * 2;    // up to 256 rows x 128 slots bf16 = 64 KB
@@ -1035,13 +1037,14 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             if (c[u] == 0.f) continue;  // padded heads, or nothing to correct
+            // packed bf16 FMA, one rounding: -c (bf16) * P + dS'
+            const __nv_bfloat162 nc = __float2bfloat162_rn(-c[u]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const float2 d2 =
-                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[u][k]));
-              const float2 p2 =
-                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pw[u][k]));
-              dw[u][k] = pack_bf16x2(fmaf(-c[u], p2.x, d2.x), fmaf(-c[u], p2.y, d2.y));
+              const __nv_bfloat162 r =
+                  __hfma2(nc, *reinterpret_cast<const __nv_bfloat162*>(&pw[u][k]),
+                          *reinterpret_cast<const __nv_bfloat162*>(&dw[u][k]));
+              dw[u][k] = *reinterpret_cast<const uint32_t*>(&r);
             }
             asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a[u]), "r"(dw[u][0]),
                          "r"(dw[u][1]), "r"(dw[u][2]), "r"(dw[u][3])
