@@ -103,14 +103,14 @@ typedef struct {
  *   - Resolution 2^-32 (2.3e-10) per add; every dkv element must stay
  *     below 2^31 in magnitude.
  *   - Range check: every element of KV row r receives n_r adds (the valid
- *     slots naming r), each at most m_r in magnitude, so its sum is bounded
- *     by n_r * m_r.  The backward counts n_r, tracks m_r, and where
- *     n_r * m_r reaches 2^31 the row may have wrapped: the call still
- *     completes, and the next dsa_device_status returns DSA_ERR_RANGE
- *     (dkv is then not to be trusted).  The bound is conservative: no row
- *     that passes it can have wrapped.
+ *     slots naming r), each at most m in magnitude (m: the largest |add|
+ *     of the call), so its sum is bounded by n_r * m.  The backward counts
+ *     n_r, tracks m, and where n_r * m reaches 2^31 the row may have
+ *     wrapped: the call still completes, and the next dsa_device_status
+ *     returns DSA_ERR_RANGE (dkv is then not to be trusted).  The bound is
+ *     conservative: no row that passes it can have wrapped.
  *   - The dkv accumulator in the workspace takes 8 bytes per element
- *     instead of 4, plus 8 bytes per KV row for the range check
+ *     instead of 4, plus 4 bytes per KV row for the range check
  *     (dsa_bwd_workspace_bytes accounts for both).
  * Ignored by dsa_fwd.
  */

@@ -70,7 +70,7 @@ BwdWorkspace bwd_workspace_layout(const Problem& p) {
   w.dkv_acc = off; off = up(off + static_cast<size_t>(p.S_kv) * p.d_qk * (p.deterministic ? 8 : 4));
   if (p.deterministic) {  // the range bound per KV row, zeroed with the accumulator
     w.det_count = off; off = up(off + static_cast<size_t>(p.S_kv) * 4);
-    w.det_max = off;   off = up(off + static_cast<size_t>(p.S_kv) * 4);
+    w.det_max = off;   off = up(off + 4);
   }
   w.zero_bytes = off;
   w.idxc = off;    off = up(off + static_cast<size_t>(p.T) * p.W * 4);
@@ -1062,6 +1062,7 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
     const int sp = warp & 3, quarter = warp >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
     const uint64_t keep = l2_evict_last();
+    uint32_t vmax = 0;  // kDet: largest |v| added by this thread (fp32 bits)
     int gb = 0;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
       const int Kt = count[t];
@@ -1092,10 +1093,9 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
                 if (s < nvalid) {
                   const float f = __uint_as_float(v[s]);
                   red_add_fixed32(dst + o, f, keep);
-                  // largest |v| added to the row (non-negative floats order
+                  // largest |v| this thread adds (non-negative floats order
                   // like their bit patterns; NaN counts as the largest)
-                  const uint32_t mx = redux_max_u32(__float_as_uint(fabsf(f)));
-                  if (lane == 0) atomicMax(row_max + o / kD, mx);
+                  vmax = max(vmax, __float_as_uint(fabsf(f)));
                 }
               }
             }
@@ -1129,6 +1129,10 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         __syncwarp();
       }
     }
+    if constexpr (kDet) {  // one atomic per warp for the range check
+      const uint32_t mx = redux_max_u32(vmax);
+      if (lane == 0 && mx != 0) atomicMax(row_max, mx);
+    }
   }
 
   tc_fence_before();
@@ -1154,19 +1158,19 @@ k_dkv_cast(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dkv, long 
 }
 
 // The fixed-point accumulator (int64, units of 2^-32) -> bf16 dkv.  Every
-// element of row r received row_refs[r] adds, each at most row_max[r] in
-// magnitude, so its sum stayed inside the accumulator's +-2^31 when their
-// product is below 2^31; otherwise the row may have wrapped, and the error
-// word says so (DSA_ERR_RANGE).
+// element of row r received row_refs[r] adds, each at most *vmax (the
+// largest |add| of the whole call) in magnitude, so its sum stayed inside the
+// accumulator's +-2^31 when their product is below 2^31; otherwise the row
+// may have wrapped, and the error word says so (DSA_ERR_RANGE).
 __global__ void __launch_bounds__(256)
 k_dkv_cast_fixed(const long long* __restrict__ acc, __nv_bfloat16* __restrict__ dkv, long long n8,
                  const unsigned int* __restrict__ row_refs,
-                 const unsigned int* __restrict__ row_max, int D) {
+                 const unsigned int* __restrict__ vmax, int D) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n8) return;
   if ((8 * i) % D == 0) {  // first piece of a row
     const long long r = 8 * i / D;
-    const float bound = static_cast<float>(row_refs[r]) * __uint_as_float(row_max[r]);
+    const float bound = static_cast<float>(row_refs[r]) * __uint_as_float(*vmax);
     if (!(bound < 2147483648.0f)) atomicCAS(&g_err_bwd, 0u, kErrDetRange);
   }
   float f[8];

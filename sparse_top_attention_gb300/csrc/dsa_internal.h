@@ -27,7 +27,7 @@ struct Problem {
 struct BwdWorkspace {
   size_t dkv_acc;   // fp32 [S_kv, 576], or int64 [S_kv, 576] in 2^-32 units when deterministic
   size_t det_count; // u32 [S_kv]     deterministic only: valid slots naming each KV row
-  size_t det_max;   // u32 [S_kv]     deterministic only: largest |add| per row (fp32 bits)
+  size_t det_max;   // u32 [1]        deterministic only: largest |add| of the call (fp32 bits)
   size_t zero_bytes;  // end of the region zeroed before the backward (from dkv_acc = 0)
   size_t idxc;      // int32 [T, W]   compacted rows
   size_t count;     // int32 [T]
