@@ -480,35 +480,43 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     cp_async_wait_all();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ UMMA issue
+    // The issuing thread's bookkeeping sits between MMAs: ring stages are
+    // followed incrementally and descriptors stepped by constants (the start
+    // address field counts 16-byte units).
     if (lane == 0) {
       const uint32_t idSdP = idesc_bf16(128, 2 * kHG, false, false);  // [S^T | dP^T]
       const uint32_t idS = idesc_bf16(128, kHG, false, false);         // S^T, rope part
       const uint32_t idQ = idesc_bf16(128, kHG, true, false);  // dQ^T: A MN-major, B K-major
       const uint32_t idQ2 = idesc_bf16(128, 2 * kHG, true, false);  // rope tile: B = [dS'; P]
-      int it = 0, gb = 0, gs = 0;
+      const uint32_t kvfull0 = smem_u32(&m.kv_full[0]), kvfree0 = smem_u32(&m.kv_free[0]);
+      const uint32_t qdfull0 = smem_u32(&m.qd_full[0]), qdfree0 = smem_u32(&m.qd_free[0]);
+      const uint64_t dkv0 = sdesc_sw128(sbase + kOffKV, 16, 1024);   // KV chunk, K-major
+      const uint64_t dqd0 = sdesc_sw128(sbase + kOffQD, 16, 1024);   // (Q, dO) stage, K-major
+      const uint64_t dsp0 = sdesc_sw128(sbase + kOffSP, 16, 1024);   // [dS'; P], K-major
+      int it = 0, gb = 0;
+      int qs = 0, qn = 0;  // ring stage of the next S / dP step and its fill count
       for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
         const int t = u / G;
         const int Kt = count[t];
         if (Kt == 0) continue;
         const int nblk = (Kt + kBlk - 1) / kBlk;
         for (int b = 0; b < nblk; ++b, ++gb) {
-          for (int i = 0; i < kCh; ++i, ++gs) {
+#pragma unroll
+          for (int i = 0; i < kCh; ++i) {
             const int pos = pos_of_step<kRope>(i);
-            const int x = dchunk_of_pos<kRope>(pos);
-            const int s = gs % kStages, n = gs / kStages;
-            mbar_wait(smem_u32(&m.kv_full[pos]), gb & 1, fs, 3);
-            mbar_wait(smem_u32(&m.qd_full[s]), n & 1, fs, 2);
+            mbar_wait(kvfull0 + 8 * pos, gb & 1, fs, 3);
+            mbar_wait(qdfull0 + 8 * qs, qn & 1, fs, 2);
             fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
             tc_fence_after();
+            // V chunks: S and dP in one N = 128 MMA (B rows: the Q heads, then
+            // the dO heads); the rope chunk adds to S only.
+            const uint64_t a0 = dkv0 + static_cast<uint64_t>(pos * (kKVChunk >> 4));
+            const uint64_t b0 = dqd0 + static_cast<uint64_t>(qs * (kStage >> 4));
+            const uint32_t id = dchunk_of_pos<kRope>(pos) < 8 ? idSdP : idS;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = sdesc_sw128(sbase + kOffKV + pos * kKVChunk + k * 32, 16, 1024);
-              // V chunks: S and dP in one N = 128 MMA (B rows: the Q heads,
-              // then the dO heads); the rope chunk adds to S only.
-              const uint64_t bqd = sdesc_sw128(sbase + kOffQD + s * kStage + k * 32, 16, 1024);
-              umma_ss(tmem + kColS, a, bqd, x < 8 ? idSdP : idS, (i | k) != 0);
-            }
-            umma_commit(smem_u32(&m.qd_free[s]));
+            for (int k = 0; k < 4; ++k) umma_ss(tmem + kColS, a0 + 2 * k, b0 + 2 * k, id, (i | k) != 0);
+            umma_commit(qdfree0 + 8 * qs);
+            if (++qs == kStages) { qs = 0; ++qn; }
           }
           umma_commit(smem_u32(&m.s_full));
           // dS' and P of this block; for the first block of an item this also
@@ -519,29 +527,34 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
           // is [dS'; P] (N = 2 kHG), so its second half accumulates
           // KV_rope^T . P^T; its 64 filler rows (d 576..639) read the ones
           // tile, so they accumulate sigma = sum over slots of dS' (and of P).
+          // (Its LBO reaches the ones tile from each step's start, so the LBO
+          // field falls by what the start field gains.)
+#pragma unroll 1
           for (int jj = 0; jj < kDT; ++jj) {
             const int j = kRope ? ((jj == 0) ? 4 : jj - 1) : jj;
             const int pos0 = (j == 4) ? 0 : (kRope ? 1 + 2 * j : 2 * j);
+            const uint32_t a_addr = kOffKV + pos0 * kKVChunk;
+            const uint64_t da = (j == 4) ? sdesc_sw128(sbase + a_addr, kOffOnes - a_addr, 1024)
+                                         : sdesc_sw128(sbase + a_addr, kKVChunk, 1024);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t a_addr = kOffKV + pos0 * kKVChunk + kk * 2048;
-              const uint32_t lbo = (j == 4) ? static_cast<uint32_t>(kOffOnes) - a_addr : kKVChunk;
-              const uint64_t a = sdesc_sw128(sbase + a_addr, lbo, 1024);
+              const uint64_t step = static_cast<uint64_t>(kk * (2048 >> 4));
+              const uint64_t a = (j == 4) ? da + step - (step << 16) : da + step;
               const uint64_t bs =
-                  sdesc_sw128(sbase + kOffSP + (kk >> 2) * (2 * kHChunk) + (kk & 3) * 32, 16, 1024);
+                  dsp0 + static_cast<uint64_t>((kk >> 2) * ((2 * kHChunk) >> 4) + (kk & 3) * 2);
               umma_ss(tmem + kColdQ + j * kHG, a, bs, j == 4 ? idQ2 : idQ, (b | kk) != 0);
             }
-            umma_commit(smem_u32(&m.kv_free[pos0]));
-            if (j != 4) umma_commit(smem_u32(&m.kv_free[pos0 + 1]));
+            umma_commit(kvfree0 + 8 * pos0);
+            if (j != 4) umma_commit(kvfree0 + 8 * (pos0 + 1));
           }
           if constexpr (!kRope) {
             // sigma without a rope tile: rows 0..63 of A are the ones tile,
             // rows 64..127 (never read) the first dS' rows.
+            const uint64_t a = sdesc_sw128(sbase + kOffOnes, kOffSP - kOffOnes, 1024);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t a = sdesc_sw128(sbase + kOffOnes, kOffSP - kOffOnes, 1024);
               const uint64_t bs =
-                  sdesc_sw128(sbase + kOffSP + (kk >> 2) * (2 * kHChunk) + (kk & 3) * 32, 16, 1024);
+                  dsp0 + static_cast<uint64_t>((kk >> 2) * ((2 * kHChunk) >> 4) + (kk & 3) * 2);
               umma_ss(tmem + kColTail, a, bs, idQ, (b | kk) != 0);
             }
           }
@@ -957,8 +970,18 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
     __syncwarp();
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
+      // Descriptors are built once and stepped by constants (the start
+      // address field counts 16-byte units); accumulators and A stages
+      // alternate by parity.
       const uint32_t id = idesc_bf16(128, kBlk, true, true);
-      int gb = 0;
+      const uint64_t da0 = sdesc_sw128(sbase + kOffA, a_half, 1024);   // Q^T / dO^T, MN-major
+      const uint64_t db0 = sdesc_sw128(sbase + kOffB, b_half, 1024);   // [dS''; P], MN-major
+      const uint64_t a_dO = static_cast<uint64_t>((2 * a_half) >> 4);  // dO^T after the two Q^T boxes
+      const uint64_t b_P = static_cast<uint64_t>((HP * 128) >> 4);     // P rows after the dS'' rows
+      const int nk = HP / 16;
+      const uint32_t afull0 = smem_u32(&m.a_full[0]), aempty0 = smem_u32(&m.a_empty[0]);
+      const uint32_t dfull0 = smem_u32(&m.d_full[0]), dempty0 = smem_u32(&m.d_empty[0]);
+      int gb = 0, use = 0, st = 0;  // A stage / accumulator of the next d tile, and its use count
       for (int t = blockIdx.x; t < T; t += gridDim.x) {
         const int Kt = count[t];
         if (Kt == 0) continue;
@@ -966,28 +989,22 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         for (int b = 0; b < nblk; ++b, ++gb) {
           mbar_wait(smem_u32(&m.b_fixed), gb & 1, fs, 22);
           for (int n = 0; n < kNT; ++n) {
-            const int u = gb * kNT + n, st = u & 1, use = u >> 1;
-            mbar_wait(smem_u32(&m.a_full[st]), use & 1, fs, 23);
-            if (use > 0) mbar_wait(smem_u32(&m.d_empty[st]), (use - 1) & 1, fs, 24);
+            mbar_wait(afull0 + 8 * st, use & 1, fs, 23);
+            if (use > 0) mbar_wait(dempty0 + 8 * st, (use - 1) & 1, fs, 24);
             tc_fence_after();
-            const uint32_t base = sbase + kOffA + st * kAStage;
+            const uint64_t da = da0 + static_cast<uint64_t>((st * kAStage) >> 4);
             const uint32_t d_t = tmem + st * kBlk;
-            // dS' . Q part: A = Q^T (M = d), B = scratch rows 0..HP-1
-            for (int kk = 0; kk < HP / 16; ++kk) {
-              const uint64_t a = sdesc_sw128(base + kk * 2048, a_half, 1024);
-              const uint64_t bb = sdesc_sw128(sbase + kOffB + kk * 2048, b_half, 1024);
-              umma_ss(d_t, a, bb, id, kk != 0);
-            }
+            // dS'' . Q part: A = Q^T (M = d), B = scratch rows 0..HP-1
+            for (int kk = 0; kk < nk; ++kk)
+              umma_ss(d_t, da + 128 * kk, db0 + 128 * kk, id, kk != 0);
             if (n < 4) {  // P . dO part: A = dO^T, B = scratch rows HP..2HP-1
-              for (int kk = 0; kk < HP / 16; ++kk) {
-                const uint64_t a = sdesc_sw128(base + 2 * a_half + kk * 2048, a_half, 1024);
-                const uint64_t bb =
-                    sdesc_sw128(sbase + kOffB + HP * 128 + kk * 2048, b_half, 1024);
-                umma_ss(d_t, a, bb, id, 1);
-              }
+              for (int kk = 0; kk < nk; ++kk)
+                umma_ss(d_t, da + a_dO + 128 * kk, db0 + b_P + 128 * kk, id, 1);
             }
-            umma_commit(smem_u32(&m.a_empty[st]));
-            umma_commit(smem_u32(&m.d_full[st]));
+            umma_commit(aempty0 + 8 * st);
+            umma_commit(dfull0 + 8 * st);
+            st ^= 1;
+            use += st == 0;
           }
           umma_commit(smem_u32(&m.b_empty));
         }
