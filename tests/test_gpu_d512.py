@@ -20,6 +20,7 @@ SMALL = [
     ("flash_T512_h128", dict(T=512, H=128, topk=512, compact=False, seed=2001)),
     ("flash_T512_h64_compact", dict(T=512, H=64, topk=512, compact=True, seed=2002)),
     ("ragged_T300_h24", dict(T=300, H=24, topk=128, compact=True, seed=2003)),
+    ("flash_T512_h16", dict(T=512, H=16, topk=512, compact=False, seed=2006)),
 ]
 
 

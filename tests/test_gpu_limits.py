@@ -1,7 +1,9 @@
 """GPU parity at the limits of the sizes: no tokens, one token, the widest and
 narrowest index rows, a single KV row, one head, a ragged head group
 (H = 33) and a head count that leaves a single real head in the last
-64-head group of both the forward and the backward (H = 65)."""
+64-head group of both the forward and the backward (H = 65).  The widest rows
+also run at 16 and 24 heads, where the forward uses its 16- and 32-head
+instances, whose KV ring wraps many times within one item (16 blocks)."""
 import numpy as np
 import pytest
 import torch
@@ -23,6 +25,8 @@ CASES = [
     ("h33_ragged_head_group", (200, 33, 900, 300, 300, True)),
     ("h65_one_head_in_last_group", (200, 65, 900, 300, 300, False)),
     ("h128", (200, 128, 900, 300, 300, False)),
+    ("h16_widest_rows", (64, 16, 3000, 2048, 2048, False)),
+    ("h24_widest_rows_compact", (48, 24, 3000, 2048, 2048, True)),
 ]
 
 
