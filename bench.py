@@ -268,9 +268,9 @@ def run_ours(args, rank, world, local):
     if dsa.device_status() != 0:
         raise RuntimeError("device status not ok after warm-up")
 
-    # Kernel launches per step: fwd 1; preprocess 2 (k_compact, k_bwd_pre; plus a
-    # driver memset); main 1 (k_bwd_dq); finalize 3 (k_bwd_dkv, k_dkv_cast, k_dsink).
-    launches_per_step = 1 + 2 + 1 + 3
+    # Kernel launches per step: fwd 1; preprocess 1 (k_compact, plus a driver
+    # memset); main 1 (k_bwd_dq); finalize 3 (k_bwd_dkv, k_dkv_cast, k_dsink).
+    launches_per_step = 1 + 1 + 1 + 3
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()

@@ -158,9 +158,9 @@ size_t dsa_bwd_workspace_bytes(const dsa_problem_t* problem);
  *   dsink  fp32 [H]          must be NULL exactly when sink is NULL
  * workspace: device memory of at least dsa_bwd_workspace_bytes(problem)
  * bytes, 256-byte aligned.  It is overwritten.
- * The call queues, in order: a memset, slot compaction, the delta
- * preprocess, the dq kernel, the dkv kernel, the dkv cast, and the d_sink
- * reduce.
+ * The call queues, in order: a memset, slot compaction, the dq kernel
+ * (which also forms rowsum(dout * out) per row), the dkv kernel, the dkv
+ * cast, and the d_sink reduce.
  * Delta.  The gradients use the exact delta[t,h] = sum_j P_j dP_j, the
  * accurate form in the cuDNN page's "Not addressed" table, not only
  * rowsum(dout * out) of the bf16 out (the FlashAttention identity), whose
@@ -179,10 +179,10 @@ dsa_status_t dsa_bwd(const dsa_problem_t* problem, const void* q, const void* kv
  * want to time or interleave them.  Each takes exactly dsa_bwd's arguments
  * and checks them the same way.  They must run in this order, on one stream
  * and with one workspace; together they equal one dsa_bwd call.
- *   dsa_bwd_preprocess  memset of the dkv accumulator, slot compaction and
- *                       the delta preprocess
- *   dsa_bwd_main        P recompute, dS and dq for every 64-head group, which
- *                       also stores the dS' and P tiles into the workspace
+ *   dsa_bwd_preprocess  memset of the dkv accumulator and slot compaction
+ *   dsa_bwd_main        rowsum(dout * out), P recompute, dS and dq for every
+ *                       64-head group, which also stores the dS' and P tiles
+ *                       into the workspace
  *   dsa_bwd_finalize    the dkv tile GEMM over all heads with its
  *                       scatter-add, the dkv fp32 -> bf16 cast and the
  *                       d_sink reduce

@@ -3,10 +3,11 @@
 // Kernels, queued in order on the caller's stream:
 //   memset      dkv accumulator <- 0 (fp32, or int64 fixed point)
 //   k_compact   a1: valid KV rows of every token, in slot order, and counts
-//   k_bwd_pre   b1: delta = rowsum(dout * out), lse*log2(e), gate and the
-//               per-(t,h) d_sink terms (FlashAttention "dpsum" preprocess)
-//   k_bwd_dq    b2-b5: per (token, 64-head group; 32 heads when H <= 32)
-//               recompute P, form dS, accumulate dQ in TMEM and store dq;
+//   k_bwd_dq    b1-b5: per (token, 64-head group; 32 heads when H <= 32)
+//               delta_a = rowsum(dout * out) (the FlashAttention "dpsum"
+//               preprocess, done by the softmax warps while the item's first
+//               S / dP GEMMs run), recompute P, form dS, accumulate dQ in TMEM
+//               and store dq with the exact-delta correction;
 //               write the dS' and P
 //               tiles of every 128-slot block to a bf16 scratch.  One
 //               persistent CTA per SM walks the (token, group) items.
@@ -75,8 +76,6 @@ BwdWorkspace bwd_workspace_layout(const Problem& p) {
   w.zero_bytes = off;
   w.idxc = off;    off = up(off + static_cast<size_t>(p.T) * p.W * 4);
   w.count = off;   off = up(off + static_cast<size_t>(p.T) * 4);
-  w.lse2 = off;    off = up(off + TH * 4);
-  w.gate = off;    off = up(off + TH * 4);
   w.delta = off;   off = up(off + TH * 4);
   w.dsink_t = off; off = up(off + TH * 4);
   w.cfix = off;    off = up(off + TH * 4);
@@ -111,66 +110,6 @@ k_compact(const int32_t* __restrict__ topk_idxs, const int32_t* __restrict__ top
   if (threadIdx.x == 0) count_out[t] = n;
   if (row_refs != nullptr)  // the list is complete: compact_token ends on a barrier
     for (int i = threadIdx.x; i < n; i += kCompactThreads) atomicAdd(row_refs + list[i], 1u);
-}
-
-// ------------------------------------------------------------------ b1
-
-// One warp per (t, h) row: delta = sum_d dout*out over the 512 V columns.
-__global__ void __launch_bounds__(256)
-k_bwd_pre(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
-          const float* __restrict__ lse, const float* __restrict__ sink,
-          const int32_t* __restrict__ count, float* __restrict__ lse2_o,
-          float* __restrict__ gate_o, float* __restrict__ delta_o, float* __restrict__ dsink_t,
-          int T, int H, int residual) {
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= static_cast<long long>(T) * H) return;
-  const int t = static_cast<int>(row / H), h = static_cast<int>(row - static_cast<long long>(t) * H);
-  const uint4* o4 = reinterpret_cast<const uint4*>(out + row * kDv);
-  const uint4* d4 = reinterpret_cast<const uint4*>(dout + row * kDv);
-  float acc = 0.f;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint4 a = o4[lane + 32 * i], b = d4[lane + 32 * i];
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 fa = __bfloat1622float2(a2[k]), fb = __bfloat1622float2(b2[k]);
-      acc = fmaf(fa.x, fb.x, acc);
-      acc = fmaf(fa.y, fb.y, acc);
-    }
-  }
-  if (residual) {  // delta from out + its rounding residual (about fp32 O)
-    const uint4* l4 = reinterpret_cast<const uint4*>(out + static_cast<size_t>(T) * H * kDv + row * kDv);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint4 a = l4[lane + 32 * i], b = d4[lane + 32 * i];
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 fa = __bfloat1622float2(a2[k]), fb = __bfloat1622float2(b2[k]);
-        acc = fmaf(fa.x, fb.x, acc);
-        acc = fmaf(fa.y, fb.y, acc);
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
-    const bool empty = count[t] == 0;
-    const float l = lse[row];
-    const float sk = sink != nullptr ? sink[h] : -INFINITY;
-    // An empty row has no attention term: the sink holds the whole
-    // denominator (p_sink = 1) and P is zero.
-    const float gate = empty ? 0.f : stable_sigmoid(l - sk);
-    const float p_sink = empty ? 1.f : stable_sigmoid(sk - l);
-    lse2_o[row] = empty ? 0.f : l * kLog2e;
-    gate_o[row] = gate;
-    delta_o[row] = acc;
-    dsink_t[row] = -p_sink * acc;
-  }
 }
 
 // ------------------------------------------------------------------ b2-b4: dq, dS', P
@@ -314,8 +253,9 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
          const __grid_constant__ CUtensorMap tm_sp, const __grid_constant__ CUtensorMap tm_kv,
          const __nv_bfloat16* __restrict__ kv,
          const int32_t* __restrict__ idxc, const int32_t* __restrict__ count,
-         const float* __restrict__ lse2_g, const float* __restrict__ gate_g,
-         const float* __restrict__ delta_g, const __nv_bfloat16* __restrict__ out,
+         const float* __restrict__ lse, const float* __restrict__ sink,
+         const __nv_bfloat16* __restrict__ dout, int residual, const __nv_bfloat16* __restrict__ out,
+         float* __restrict__ delta_g,
          float* __restrict__ dsink_t, float* __restrict__ cfix_g,
          __nv_bfloat16* __restrict__ dq, int T, int H, int W,
          float scale, int G, int G32, int box_heads, int nbmax) {
@@ -577,29 +517,107 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     const float sl2 = scale * kLog2e;
     const size_t spr = static_cast<size_t>(64) * G32;  // scratch rows per (token, block)
     const int row = (warp & 3) * 32 + lane, hb = (warp >> 2) * kHT;
+    const size_t lo_off = residual ? static_cast<size_t>(T) * H * kDv : 0;  // residual half
+    // delta_a = rowsum(dout * out) of an item's heads (with out's rounding
+    // residual when the forward stored it): to dst[h * stride] for every head
+    // of the group (0 for padded heads) when `all`, else for the real heads
+    // only.  Warp w takes heads w, w + 8, ..., two per round, so that eight
+    // 16-byte loads per lane are in flight; lane l reads pieces l and l + 32
+    // of a row, so each warp load covers 512 contiguous bytes.  The softmax
+    // warps compute the next item's values while they wait for the last
+    // S / dP GEMMs of this one (and a CTA's first item's before it starts).
+    auto item_delta = [&](int t, int h0, int nh, float* dst, int stride, bool all) {
+      const size_t base = (static_cast<size_t>(t) * H + h0) * kDv;
+      auto dot8 = [](const uint4& a, const uint4& b, float acc) {
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 fa = __bfloat1622float2(a2[k]), fb = __bfloat1622float2(b2[k]);
+          acc = fmaf(fa.x, fb.x, acc);
+          acc = fmaf(fa.y, fb.y, acc);
+        }
+        return acc;
+      };
+      // the out rows, then (with the residual flag) a second pass over the
+      // residual rows, so that only eight loads per lane are live at a time
+#pragma unroll 1
+      for (int pass = 0; pass < (residual ? 2 : 1); ++pass) {
+        const size_t ob = base + (pass ? lo_off : 0);
+#pragma unroll
+        for (int r = 0; r < kHG / 16; ++r) {
+          uint4 o[2][2], d[2][2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int hh = warp + 8 * (2 * r + j);
+            const bool ok = hh < nh;
+            const uint4* o4 = reinterpret_cast<const uint4*>(out + ob + static_cast<size_t>(hh) * kDv);
+            const uint4* d4 = reinterpret_cast<const uint4*>(dout + base + static_cast<size_t>(hh) * kDv);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint4 z = make_uint4(0, 0, 0, 0);
+              o[j][k] = ok ? __ldg(o4 + lane + 32 * k) : z;
+              d[j][k] = ok ? __ldg(d4 + lane + 32 * k) : z;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float acc = dot8(o[j][1], d[j][1], dot8(o[j][0], d[j][0], 0.f));
+#pragma unroll
+            for (int x = 16; x > 0; x >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, x);
+            const int hh = warp + 8 * (2 * r + j);
+            if (lane == 0 && (all || hh < nh)) {
+              float* p = dst + hh * stride;
+              *p = pass ? *p + acc : acc;
+            }
+          }
+        }
+      }
+    };
     int it = 0, gb = 0;
+    bool ahead = false;  // this item's delta_a is already in delta_g
+    // this item's delta_a -> m.cd[h].y (0 for padded heads)
+    auto load_delta = [&](int t, int h0, int nh) {
+      if (ahead) {
+        if (tid < kHG) m.cd[tid].y = tid < nh ? __ldcg(delta_g + static_cast<size_t>(t) * H + h0 + tid) : 0.f;
+      } else {
+        item_delta(t, h0, nh, &m.cd[0].y, 2, true);
+      }
+      ahead = false;
+    };
     for (int u = blockIdx.x; u < n_items; u += gridDim.x) {
       const int t = u / G, h0 = (u - t * G) * kHG;
       const int nh = min(kHG, H - h0);
       const int Kt = count[t];
-      if (Kt == 0) {  // empty row: dq = 0, nothing for dkv
+      if (Kt == 0) {  // empty row: dq = 0, nothing for dkv; the sink holds the
+                      // whole denominator (p_sink = 1), so dsink_t = -delta_a
+        load_delta(t, h0, nh);
+        named_bar_sync(1, kSoftmax);
+        if (tid < nh) dsink_t[static_cast<size_t>(t) * H + h0 + tid] = -m.cd[tid].y;
         for (int v = tid; v < nh * (kD / 8); v += kSoftmax) {
           const int h = v / (kD / 8), c = v - h * (kD / 8);
           *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(t) * H + h0 + h) * kD + c * 8) =
               make_uint4(0, 0, 0, 0);
         }
+        named_bar_sync(1, kSoftmax);  // m.cd is rewritten at the next item's start
         continue;
       }
       const int nblk = (Kt + kBlk - 1) / kBlk;
+      load_delta(t, h0, nh);
+      named_bar_sync(1, kSoftmax);
       float gate_h = 0.f, dsink_h = 0.f;  // thread tid < nh: head h0 + tid, for the epilogue
       if (tid < kHG) {
         // Padded heads get gate 0, hence P = dS = 0: they add nothing anywhere.
-        const bool real = tid < nh;
-        const size_t r = static_cast<size_t>(t) * H + h0 + tid;
-        gate_h = real ? gate_g[r] : 0.f;
-        dsink_h = real ? dsink_t[r] : 0.f;
-        m.cd[tid] = make_float2(gate_h > 0.f ? log2f(gate_h) - lse2_g[r] : -INFINITY,
-                                real ? delta_g[r] : 0.f);
+        float x = -INFINITY;  // log2(gate) - lse * log2(e)
+        if (tid < nh) {
+          const size_t r = static_cast<size_t>(t) * H + h0 + tid;
+          const float l = lse[r];
+          const float sk = sink != nullptr ? sink[h0 + tid] : -INFINITY;
+          gate_h = stable_sigmoid(l - sk);
+          dsink_h = -stable_sigmoid(sk - l) * m.cd[tid].y;  // -p_sink * delta_a
+          if (gate_h > 0.f) x = log2f(gate_h) - l * kLog2e;
+        }
+        m.cd[tid].x = x;
       }
       named_bar_sync(1, kSoftmax);
       // Per head, this row's sum over the item's blocks of the bf16 rounding
@@ -609,6 +627,13 @@ k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 #pragma unroll
       for (int i = 0; i < kHT / 2; ++i) eacc[i] = __float2bfloat162_rn(0.f);
       for (int b = 0; b < nblk; ++b, ++gb) {
+        if (b == nblk - 1 && u + static_cast<int>(gridDim.x) < n_items) {
+          // the next item's delta_a, while this block's S / dP GEMMs run
+          const int un = u + gridDim.x, tn = un / G, hn = (un - tn * G) * kHG;
+          item_delta(tn, hn, min(kHG, H - hn), delta_g + static_cast<size_t>(tn) * H + hn, 1,
+                     false);
+          ahead = true;
+        }
         mbar_wait(smem_u32(&m.s_full), gb & 1, fs, 7);
         tc_fence_after();
         const bool valid = b * kBlk + row < Kt;
@@ -1292,8 +1317,6 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
       p.deterministic ? reinterpret_cast<unsigned int*>(base + L.det_max) : nullptr;
   int32_t* idxc = reinterpret_cast<int32_t*>(base + L.idxc);
   int32_t* count = reinterpret_cast<int32_t*>(base + L.count);
-  float* lse2 = reinterpret_cast<float*>(base + L.lse2);
-  float* gate = reinterpret_cast<float*>(base + L.gate);
   float* delta = reinterpret_cast<float*>(base + L.delta);
   float* dsink_t = reinterpret_cast<float*>(base + L.dsink_t);
   float* cfix = reinterpret_cast<float*>(base + L.cfix);
@@ -1303,12 +1326,6 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     if (e != cudaSuccess) return e;
     if (p.T > 0) {
       e = launch_compact(p, idx, len, idxc, count, s, row_refs);
-      if (e != cudaSuccess) return e;
-      const long long rows = static_cast<long long>(p.T) * p.H;
-      k_bwd_pre<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse,
-          sink, count, lse2, gate, delta, dsink_t, p.T, p.H, p.delta_residual ? 1 : 0);
-      e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
   }
@@ -1336,8 +1353,9 @@ cudaError_t launch_bwd(const Problem& p, const void* q, const void* kv, const in
     const long long items = static_cast<long long>(p.T) * G;
     const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
     kern<<<grid, kThreads, smem, s>>>(
-        tm_q, tm_do, tm_sp_st, tm_kv, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse2,
-        gate, delta, static_cast<const __nv_bfloat16*>(out), dsink_t, cfix,
+        tm_q, tm_do, tm_sp_st, tm_kv, static_cast<const __nv_bfloat16*>(kv), idxc, count, lse,
+        sink, static_cast<const __nv_bfloat16*>(dout), p.delta_residual ? 1 : 0,
+        static_cast<const __nv_bfloat16*>(out), delta, dsink_t, cfix,
         static_cast<__nv_bfloat16*>(dq), p.T, p.H, p.W, p.scale, G, G32, box_heads, nbmax);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

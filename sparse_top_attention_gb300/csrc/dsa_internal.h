@@ -31,10 +31,8 @@ struct BwdWorkspace {
   size_t zero_bytes;  // end of the region zeroed before the backward (from dkv_acc = 0)
   size_t idxc;      // int32 [T, W]   compacted rows
   size_t count;     // int32 [T]
-  size_t lse2;      // fp32 [T, H]    lse * log2(e), 0 for empty rows
-  size_t gate;      // fp32 [T, H]    sigma(lse - sink), 0 for empty rows
-  size_t delta;     // fp32 [T, H]    rowsum(dout * out)
-  size_t dsink_t;   // fp32 [T, H]    -p_sink * delta (the exact delta once the main stage ran)
+  size_t delta;     // fp32 [T, H]    rowsum(dout * out), written by the main stage one item ahead
+  size_t dsink_t;   // fp32 [T, H]    -p_sink * delta (exact delta), from the main stage
   size_t cfix;      // fp32 [T, H]    scale * (exact delta - delta from out), from the main stage
   size_t sp;        // bf16 [T, nbmax, 64G, 128]: per (token, 128-slot block) the
                     // dS' rows (32G heads) then the P rows (32G heads), slots
