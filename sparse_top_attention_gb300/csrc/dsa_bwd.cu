@@ -1012,20 +1012,27 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         if (Kt == 0) continue;
         const int nblk = (Kt + kBlk - 1) / kBlk;
         for (int b = 0; b < nblk; ++b, ++gb) {
-          mbar_wait(smem_u32(&m.b_fixed), gb & 1, fs, 22);
+          // The P rows are final as loaded: the first tile's P . dO part runs
+          // while the fixup warps still correct the dS' rows.
+          mbar_wait(smem_u32(&m.b_full), gb & 1, fs, 22);
           for (int n = 0; n < kNT; ++n) {
             mbar_wait(afull0 + 8 * st, use & 1, fs, 23);
             if (use > 0) mbar_wait(dempty0 + 8 * st, (use - 1) & 1, fs, 24);
             tc_fence_after();
             const uint64_t da = da0 + static_cast<uint64_t>((st * kAStage) >> 4);
             const uint32_t d_t = tmem + st * kBlk;
+            // P . dO part (V tiles): A = dO^T, B = scratch rows HP..2HP-1
+            if (n < 4) {
+              for (int kk = 0; kk < nk; ++kk)
+                umma_ss(d_t, da + a_dO + 128 * kk, db0 + b_P + 128 * kk, id, kk != 0);
+            }
+            if (n == 0) {
+              mbar_wait(smem_u32(&m.b_fixed), gb & 1, fs, 27);
+              tc_fence_after();
+            }
             // dS'' . Q part: A = Q^T (M = d), B = scratch rows 0..HP-1
             for (int kk = 0; kk < nk; ++kk)
-              umma_ss(d_t, da + 128 * kk, db0 + 128 * kk, id, kk != 0);
-            if (n < 4) {  // P . dO part: A = dO^T, B = scratch rows HP..2HP-1
-              for (int kk = 0; kk < nk; ++kk)
-                umma_ss(d_t, da + a_dO + 128 * kk, db0 + b_P + 128 * kk, id, 1);
-            }
+              umma_ss(d_t, da + 128 * kk, db0 + 128 * kk, id, n < 4 || kk != 0);
             umma_commit(aempty0 + 8 * st);
             umma_commit(dfull0 + 8 * st);
             st ^= 1;
