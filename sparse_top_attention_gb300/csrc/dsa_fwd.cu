@@ -460,29 +460,38 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
         uint32_t r0[kHT];
         tmem_ld_n<kHT>(tmem + lane_base + hb, r0);
         const bool valid = b * kBlk + row < Kt;
-        float s[kHT];
-#pragma unroll
-        for (int i = 0; i < kHT; ++i) s[i] = valid ? __uint_as_float(r0[i]) * sl2 : -INFINITY;
         // Lazy rescale: a head keeps its shift unless the block's maximum
         // exceeds it by more than 2^8; the final normalisation uses the same
-        // shift for O and l.  The column maxima are only needed when some
-        // score is that far above its head's shift (always in the first
-        // block), so one vote decides whether to compute them.
-        bool above = false;
+        // shift for O and l.  P is computed with the current shifts first:
+        // a score that far above its head's shift shows as p > 2^8 (always
+        // in an item's first block, whose shifts are -inf).  Only then are
+        // the scores read again from TMEM (this block's S^T stays there
+        // until its P.V is issued), the column maxima formed and P redone.
         const float4* mu4 = reinterpret_cast<const float4*>(m.m_used + hb);
+        float p[kHT];
+        bool above = false;
 #pragma unroll
         for (int i = 0; i < kHT; i += 4) {
           const float4 mu = mu4[i / 4];
-          above |= (s[i] > mu.x + 8.f) | (s[i + 1] > mu.y + 8.f) | (s[i + 2] > mu.z + 8.f) |
-                   (s[i + 3] > mu.w + 8.f);
+          const float m4[4] = {mu.x, mu.y, mu.z, mu.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float sv = valid ? __uint_as_float(r0[i + k]) * sl2 : -INFINITY;
+            p[i + k] = ex2_approx(sv - m4[k]);
+            above |= p[i + k] > 256.f;
+          }
         }
         bool any = named_bar_or(1, kSoftmax, above);
         if (any) {
+          uint32_t r1[kHT];
+          tmem_ld_n<kHT>(tmem + lane_base + hb, r1);
+#pragma unroll
+          for (int i = 0; i < kHT; ++i) p[i] = valid ? __uint_as_float(r1[i]) * sl2 : -INFINITY;
           // column (per-head) maximum over the 128 gathered rows
           float* red = m.red[g & 1][warp & 3];
 #pragma unroll
           for (int i = 0; i < kHT; ++i) {
-            const float mx = warp_max(s[i]);
+            const float mx = warp_max(p[i]);
             if (i == lane) red[hb + i] = mx;
           }
           named_bar_sync(1, kSoftmax);
@@ -497,6 +506,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
             if (resc) m.m_used[tid] = mn;
           }
           any = named_bar_or(1, kSoftmax, resc);
+          // P with the new shifts (p[] holds the scores here)
+#pragma unroll
+          for (int i = 0; i < kHT; i += 4) {
+            const float4 mu = mu4[i / 4];
+            p[i] = ex2_approx(p[i] - mu.x);
+            p[i + 1] = ex2_approx(p[i + 1] - mu.y);
+            p[i + 2] = ex2_approx(p[i + 2] - mu.z);
+            p[i + 3] = ex2_approx(p[i + 3] - mu.w);
+          }
         }
         if (any) {
 #pragma unroll
@@ -520,21 +538,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
           }
           tmem_wait_st();
         }
-        // P^T row as bf16 pairs; s[] is dead after this loop.
+        // P^T row as bf16 pairs
         uint32_t pk[kHT / 2];
 #pragma unroll
-        for (int i = 0; i < kHT / 2; i += 2) {
-          const float4 mu = mu4[i / 2];
-          const float p0 = ex2_approx(s[2 * i] - mu.x);
-          const float p1 = ex2_approx(s[2 * i + 1] - mu.y);
-          const float p2 = ex2_approx(s[2 * i + 2] - mu.z);
-          const float p3 = ex2_approx(s[2 * i + 3] - mu.w);
-          lp[2 * i] += p0;
-          lp[2 * i + 1] += p1;
-          lp[2 * i + 2] += p2;
-          lp[2 * i + 3] += p3;
-          pk[i] = pack_bf16x2(p0, p1);
-          pk[i + 1] = pack_bf16x2(p2, p3);
+        for (int i = 0; i < kHT / 2; ++i) {
+          lp[2 * i] += p[2 * i];
+          lp[2 * i + 1] += p[2 * i + 1];
+          pk[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
         }
         const uint32_t pt = p_tile(g);
         if constexpr (!kPK) {
