@@ -60,7 +60,8 @@ struct Misc {
   uint64_t v_full[kMaxUnits][2];  // per V chunk of a unit
   uint64_t v_free[kMaxUnits];
   uint64_t rope_full[kMaxRope], rope_free[kMaxRope];
-  uint64_t q_full, q_free, s_full, p_full, o_done, mma_done;
+  uint64_t q_full[kChunks];  // per 64-column chunk of the Q tile
+  uint64_t q_free, s_full, p_full, o_done, mma_done;
   float red[2][4][kHG];   // per-warp column maxima, double-buffered by block parity
   alignas(16) float m_used[kHG];  // running shift per head (log2 units)
   float fac[kHG];         // rescale factor per head, then the output scale
@@ -227,7 +228,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       mbar_init(smem_u32(&m.rope_full[r]), kProducers);
       mbar_init(smem_u32(&m.rope_free[r]), 1);
     }
-    mbar_init(smem_u32(&m.q_full), 1);
+    for (int c = 0; c < kCh; ++c) mbar_init(smem_u32(&m.q_full[c]), 1);
     mbar_init(smem_u32(&m.q_free), 1);
     mbar_init(smem_u32(&m.s_full), 1);
     mbar_init(smem_u32(&m.p_full), kSoftmax);
@@ -281,11 +282,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       const int nblk = (Kt + kBlk - 1) / kBlk;
       if (tid == kQIssuer) {
         if (it > 0) mbar_wait(smem_u32(&m.q_free), (it - 1) & 1, fs, 8);
-        mbar_arrive_expect_tx(smem_u32(&m.q_full), kCh * box_heads * 128);
         const uint64_t pol = l2_evict_first();
-        for (int c = 0; c < kCh; ++c)
-          tma_load_3d_hint(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t,
-                           smem_u32(&m.q_full), pol);
+        // 64 heads (a 72 KB tile): one barrier per chunk, so that S starts on
+        // the first to land; a smaller tile: one barrier for all of it
+        if constexpr (kHG < 64) mbar_arrive_expect_tx(smem_u32(&m.q_full[0]), kCh * box_heads * 128);
+        for (int c = 0; c < kCh; ++c) {
+          const uint32_t qb = smem_u32(&m.q_full[kHG == 64 ? c : 0]);
+          if constexpr (kHG == 64) mbar_arrive_expect_tx(qb, box_heads * 128);
+          tma_load_3d_hint(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t, qb, pol);
+        }
       }
       for (int b = 0; b < nblk; ++b, ++gb) {
         // This lane's rows of the block, read once (before the wait on the
@@ -352,8 +357,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
     const uint64_t dp0 = kPK ? sdesc_sw128(p_tile(0), 16, 1024) : sdesc_sw128(p_tile(0), kKVChunk, 1024);
     constexpr bool kRopeFirst = L::kRope && !L::kPInRope;
     // S += chunk (d-chunk x) . Q chunk x^T, once the chunk has landed
+    const uint32_t qfull0 = smem_u32(&m.q_full[0]);
+    int qpar = -1;  // in an item's first block: the parity of its Q chunks' barriers
     auto s_chunk = [&](uint32_t full, uint32_t parity, uint64_t da, int x, bool first) {
       mbar_wait(full, parity, fs, 3);
+      if (qpar >= 0) mbar_wait(qfull0 + 8 * x, static_cast<uint32_t>(qpar), fs, 2);
       fence_proxy_async_smem();  // cp.async (generic proxy) -> UMMA (async proxy)
       tc_fence_after();
       const uint64_t db = dq0 + static_cast<uint64_t>((x * kQChunk) >> 4);
@@ -370,9 +378,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (Kt == 0) continue;
       const int nblk = (Kt + kBlk - 1) / kBlk;
       if (lane == 0) {
-        mbar_wait(smem_u32(&m.q_full), it & 1, fs, 2);
+        if constexpr (kHG < 64) mbar_wait(qfull0, it & 1, fs, 2);  // a small Q tile at once
         for (int b = 0; b < nblk; ++b) {
           const int g = gb + b;
+          // 64 heads: S starts on each Q chunk as it lands (first block only)
+          qpar = (kHG == 64 && b == 0) ? (it & 1) : -1;
           // rope slot of this block and its fill count (one or two slots)
           const int rs = L::kRopeSlots == 2 ? (g & 1) : 0;
           const int rw = L::kRopeSlots == 2 ? (g >> 1) : g;
