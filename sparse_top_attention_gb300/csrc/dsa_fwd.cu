@@ -91,6 +91,9 @@ struct FwdLayout {
   static constexpr bool kRope = kCh > 8;
   static constexpr int kQChunk = kHG * 128;    // one 64-column chunk of Q
   static constexpr bool kPInRope = kRope && kHG == 64;
+  // one Q barrier per 64-column chunk (measured faster only for the 72 KB
+  // tile of 64 heads at D = 576)
+  static constexpr bool kQPerChunk = kRope && kHG == 64;
   static constexpr bool kPKMajor = kHG < 64;
   static constexpr int kPTile = kPKMajor ? kHG * 256 : kKVChunk;
   static constexpr int kPBytes = kPInRope ? 0 : kPTile;
@@ -283,12 +286,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (tid == kQIssuer) {
         if (it > 0) mbar_wait(smem_u32(&m.q_free), (it - 1) & 1, fs, 8);
         const uint64_t pol = l2_evict_first();
-        // 64 heads (a 72 KB tile): one barrier per chunk, so that S starts on
-        // the first to land; a smaller tile: one barrier for all of it
-        if constexpr (kHG < 64) mbar_arrive_expect_tx(smem_u32(&m.q_full[0]), kCh * box_heads * 128);
+        // 64 heads at D = 576 (a 72 KB tile): one barrier per chunk, so that
+        // S starts on the first to land; otherwise one barrier for all of it
+        if constexpr (!L::kQPerChunk) mbar_arrive_expect_tx(smem_u32(&m.q_full[0]), kCh * box_heads * 128);
         for (int c = 0; c < kCh; ++c) {
-          const uint32_t qb = smem_u32(&m.q_full[kHG == 64 ? c : 0]);
-          if constexpr (kHG == 64) mbar_arrive_expect_tx(qb, box_heads * 128);
+          const uint32_t qb = smem_u32(&m.q_full[L::kQPerChunk ? c : 0]);
+          if constexpr (L::kQPerChunk) mbar_arrive_expect_tx(qb, box_heads * 128);
           tma_load_3d_hint(sbase + kOffQ + c * kQChunk, &tm_q, c * 64, h0, t, qb, pol);
         }
       }
@@ -378,11 +381,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUt
       if (Kt == 0) continue;
       const int nblk = (Kt + kBlk - 1) / kBlk;
       if (lane == 0) {
-        if constexpr (kHG < 64) mbar_wait(qfull0, it & 1, fs, 2);  // a small Q tile at once
+        if constexpr (!L::kQPerChunk) mbar_wait(qfull0, it & 1, fs, 2);  // the Q tile at once
         for (int b = 0; b < nblk; ++b) {
           const int g = gb + b;
-          // 64 heads: S starts on each Q chunk as it lands (first block only)
-          qpar = (kHG == 64 && b == 0) ? (it & 1) : -1;
+          // 64 heads at D = 576: S starts on each Q chunk as it lands (first
+          // block only)
+          qpar = (L::kQPerChunk && b == 0) ? (it & 1) : -1;
           // rope slot of this block and its fill count (one or two slots)
           const int rs = L::kRopeSlots == 2 ? (g & 1) : 0;
           const int rw = L::kRopeSlots == 2 ? (g >> 1) : g;
