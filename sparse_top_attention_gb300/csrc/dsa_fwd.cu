@@ -1,18 +1,19 @@
 // Sparse MLA (DSA) forward for sm_103a.
 //
-// A work item is one token t with a group of up to 64 query heads; each
-// persistent CTA processes a share of the items in turn.  The token's top-k
-// rows are gathered from the shared KV tensor, 128 rows at a time
-// ("blocks").  The contractions use 5th-gen tensor cores with fp32
-// accumulators in TMEM, in a transposed orientation: the gathered rows form
-// the UMMA M dimension (128) and the heads form N (64), so a 64-head group
-// fills a full-rate M=128 tile.
-//   S^T[slot, h]  = sum_d KV[slot, d] * Q[h, d]          (M=128, N=64, K=D)
-//   O^T[d, h]    += sum_slot V[slot, d] * P^T[slot, h]   (4 x M=128, N=64, K=128)
+// A work item is one token t with a group of query heads: 64, or 32 / 16
+// when H is that small (the narrowest group that holds H); each persistent
+// CTA processes a share of the items in turn.  The token's top-k rows are
+// gathered from the shared KV tensor, 128 rows at a time ("blocks").  The
+// contractions use 5th-gen tensor cores with fp32 accumulators in TMEM, in a
+// transposed orientation: the gathered rows form the UMMA M dimension (128)
+// and the heads form N, so any head group fills a full-rate M=128 tile.
+//   S^T[slot, h]  = sum_d KV[slot, d] * Q[h, d]          (M=128, N=HG, K=D)
+//   O^T[d, h]    += sum_slot V[slot, d] * P^T[slot, h]   (4 x M=128, N=HG, K=128)
 // with rows of D = 576 columns (512 V + 64 rope) or 512 (a template
 // parameter).  The softmax runs on S^T in registers, one thread per gathered
-// row and 32 heads, with a lazy rescale: a head's shift only moves when a score exceeds it
-// by more than 2^8.  The sink enters at the end, as sigma(lse - sink):
+// row and HG/2 heads, with a lazy rescale: a head's shift only moves when a
+// score exceeds it by more than 2^8.  The sink enters at the end, as
+// sigma(lse - sink):
 //   out = O * sigma(lse - sink) / l.
 // Sources:
 //   - flash-attention "[CuTe, SM100] Support 1..128 Q heads in sparse MLA via
@@ -24,14 +25,14 @@
 //
 // Warp roles (384 threads):
 //   warps 0-7  softmax and epilogue; thread (w, l) owns TMEM lane
-//              32 (w % 4) + l (gathered row) and heads 32 (w / 4) .. +31, so
-//              two softmax warps share each SM sub-partition's exp2 work
+//              32 (w % 4) + l (gathered row) and heads HG/2 * (w / 4) + ..,
+//              so two softmax warps share each SM sub-partition's exp2 work
 //   warp 8     TMEM allocation and the single UMMA-issuing thread
 //   warps 9-11 per item: compact the token's index row, lane 0 of warp 9
 //              loads the Q tile by TMA (3-D tensor map), then the three warps
 //              gather KV rows with cp.async into 128B-swizzled shared tiles,
 //              or a whole block of consecutive rows (the sliding window) with
-//              2-D TMA
+//              2-D TMA, into a ring of chunk slots
 // The kernel is persistent: one CTA per SM walks the (token, head group)
 // items, so an item's epilogue overlaps the next item's first gather.
 #include <cmath>
