@@ -53,8 +53,9 @@ def test_d512_deterministic_matches_atomic():
     assert rel_frob(a[1], c[1]) <= 1e-3
 
 
-def test_d512_varlen():
-    w = WL.varlen([200, 0, 333], H=64, topk=64, compact=True, seed=2004, d_qk=512)
+@pytest.mark.parametrize("H,topk,seed", [(64, 64, 2004), (8, 512, 2007)])
+def test_d512_varlen(H, topk, seed):
+    w = WL.varlen([200, 0, 333], H=H, topk=topk, compact=True, seed=seed, d_qk=512)
     out, lse, dq, dkv, dsink = run_varlen(w)
     ref, g = oracle_varlen(w)
     check_fwd(out, lse, ref, ref["count"])

@@ -19,6 +19,7 @@ CASES = [
     ([200, 0, 333, 64], 64, 64, False, 12),
     ([700, 300], 128, 512, False, 13),     # 640 slots, several 128-row blocks
     ([1, 130, 2, 257], 24, 128, True, 14),  # ragged tails, padded head group
+    ([600, 0, 250], 16, 512, False, 16),    # the 16-head forward, its KV ring wrapping
 ]
 
 
