@@ -878,10 +878,10 @@ constexpr int kOffA = kOffB + kBTile;       // 2 stages
 constexpr int kStageQ = 16 * 128 * 4;
 constexpr int kOffStage = kOffA + 2 * kAStage;
 constexpr int kOffMisc = kOffStage + 4 * kStageQ;
-constexpr uint32_t kTmemCols = 256;         // 2 accumulators of 128 columns
+constexpr uint32_t kTmemCols = 512;         // 4 accumulators of 128 columns
 
 struct Misc {
-  uint64_t b_full, b_fixed, b_empty, a_full[2], a_empty[2], d_full[2], d_empty[2], mma_done;
+  uint64_t b_full, b_fixed, b_empty, a_full[2], a_empty[2], d_full[4], d_empty[4], mma_done;
   float c[128];       // the token's per-head correction c_h (0 past H)
   uint32_t tmem_base;
   int abort_flag;
@@ -931,6 +931,8 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&m.a_full[i]), 1);
       mbar_init(smem_u32(&m.a_empty[i]), 1);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(smem_u32(&m.d_full[i]), 1);
       mbar_init(smem_u32(&m.d_empty[i]), kDrainWarps * 32);
     }
@@ -1006,7 +1008,8 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
       const int nk = HP / 16;
       const uint32_t afull0 = smem_u32(&m.a_full[0]), aempty0 = smem_u32(&m.a_empty[0]);
       const uint32_t dfull0 = smem_u32(&m.d_full[0]), dempty0 = smem_u32(&m.d_empty[0]);
-      int gb = 0, use = 0, st = 0;  // A stage / accumulator of the next d tile, and its use count
+      int gb = 0, use = 0, st = 0;  // A stage of the next d tile, and its use count
+      int sd = 0, used = 0;         // accumulator of the next d tile, and its use count
       for (int t = blockIdx.x; t < T; t += gridDim.x) {
         const int Kt = count[t];
         if (Kt == 0) continue;
@@ -1017,10 +1020,10 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
           mbar_wait(smem_u32(&m.b_full), gb & 1, fs, 22);
           for (int n = 0; n < kNT; ++n) {
             mbar_wait(afull0 + 8 * st, use & 1, fs, 23);
-            if (use > 0) mbar_wait(dempty0 + 8 * st, (use - 1) & 1, fs, 24);
+            if (used > 0) mbar_wait(dempty0 + 8 * sd, (used - 1) & 1, fs, 24);
             tc_fence_after();
             const uint64_t da = da0 + static_cast<uint64_t>((st * kAStage) >> 4);
-            const uint32_t d_t = tmem + st * kBlk;
+            const uint32_t d_t = tmem + sd * kBlk;
             // P . dO part (V tiles): A = dO^T, B = scratch rows HP..2HP-1
             if (n < 4) {
               for (int kk = 0; kk < nk; ++kk)
@@ -1034,9 +1037,11 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
             for (int kk = 0; kk < nk; ++kk)
               umma_ss(d_t, da + 128 * kk, db0 + 128 * kk, id, n < 4 || kk != 0);
             umma_commit(aempty0 + 8 * st);
-            umma_commit(dfull0 + 8 * st);
+            umma_commit(dfull0 + 8 * sd);
             st ^= 1;
             use += st == 0;
+            sd = (sd + 1) & 3;
+            used += sd == 0;
           }
           umma_commit(smem_u32(&m.b_empty));
         }
@@ -1125,7 +1130,7 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
         // to the whole warp without a shared-memory round trip per add.
         const uint32_t roff = lane < nvalid ? static_cast<uint32_t>(rows[s0 + lane]) * kD : 0u;
         for (int n = 0; n < kNT; ++n) {
-          const int u = gb * kNT + n, st = u & 1, use = u >> 1;
+          const int u = gb * kNT + n, st = u & 3, use = u >> 2;
           mbar_wait(smem_u32(&m.d_full[st]), use & 1, fs, 25);
           tc_fence_after();
           uint32_t v[32];
@@ -1155,23 +1160,44 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
             // warp then adds whole 128-float rows: 4 slots per warp, 32 lanes x
             // 4 floats each (the fast reduction pattern).
             float* stg = reinterpret_cast<float*>(smem + dkv::kOffStage) + quarter * (16 * 128);
-            const int dt = n * 128;  // first d of the tile
-            const bool lane_ok = dt + lane * 4 < kD;  // the rope tile has 64 columns
+            float* acc = static_cast<float*>(dkv_acc);
+            if (kD > 512 && n == kNT - 1) {
+              // The 64-column rope tile: only TMEM lanes 0..63 (sp 0 and 1)
+              // hold its d rows.  Those two warps stage all 32 slots at once
+              // (32 x 64 floats), and each reduction then covers two slots,
+              // lanes 0..15 one row and lanes 16..31 the next: half the
+              // staging, barriers and reductions of a full tile.
+              if (sp < 2) {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-#pragma unroll
-              for (int s = 0; s < 16; ++s) stg[s * 128 + sp * 32 + lane] = __uint_as_float(v[half * 16 + s]);
-              named_bar_sync(1 + quarter, 128);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int sl = sp * 4 + j;            // slot within the half
-                const int s = half * 16 + sl;         // slot within the quarter
-                const float4 f = *reinterpret_cast<const float4*>(stg + sl * 128 + lane * 4);
-                const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
-                if (s < nvalid && lane_ok)
-                  red_add_v4_f32_hint(static_cast<float*>(dkv_acc) + o + dt + lane * 4, f, keep);
+                for (int s = 0; s < 32; ++s) stg[s * 64 + sp * 32 + lane] = __uint_as_float(v[s]);
               }
               named_bar_sync(1 + quarter, 128);
+              const int c4 = (lane & 15) * 4;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int s = sp * 8 + 2 * j + (lane >> 4);  // slot within the quarter
+                const float4 f = *reinterpret_cast<const float4*>(stg + s * 64 + c4);
+                const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
+                if (s < nvalid) red_add_v4_f32_hint(acc + o + 512 + c4, f, keep);
+              }
+              named_bar_sync(1 + quarter, 128);
+            } else {
+              const int dt = n * 128;  // first d of the tile (a full 128-column tile)
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                for (int s = 0; s < 16; ++s) stg[s * 128 + sp * 32 + lane] = __uint_as_float(v[half * 16 + s]);
+                named_bar_sync(1 + quarter, 128);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int sl = sp * 4 + j;            // slot within the half
+                  const int s = half * 16 + sl;         // slot within the quarter
+                  const float4 f = *reinterpret_cast<const float4*>(stg + sl * 128 + lane * 4);
+                  const uint32_t o = __shfl_sync(0xffffffffu, roff, s);
+                  if (s < nvalid) red_add_v4_f32_hint(acc + o + dt + lane * 4, f, keep);
+                }
+                named_bar_sync(1 + quarter, 128);
+              }
             }
           }
         }
