@@ -1,8 +1,9 @@
 """GPU parity for the persistent kernels' scheduling.
 
-The forward and the dq kernel launch one CTA per SM; each CTA walks the
-(token, head group) items c, c + grid, ... and keeps its barrier phases in
-running counts of items, blocks and S steps.  These cases stress that
+The forward launches one CTA per SM, k_bwd_dq and k_bwd_dkv two; each CTA
+walks its items c, c + grid, ... ((token, head group) items, or tokens in
+k_bwd_dkv) and keeps its barrier phases in running counts of items, blocks
+and S steps.  These cases stress that
 bookkeeping: long runs of empty tokens (every role must skip the same items),
 fewer items than SMs, one item more than the grid, and items that differ
 widely in block count next to each other.
@@ -73,10 +74,14 @@ def test_fewer_items_than_sms():
     _check(WL.random_rows(20, 128, 2000, 640, 640, seed=4300))
 
 
-def test_one_item_more_than_the_grid():
-    """T * G = SMs + 1 items at H = 64 (one head group): CTA 0 takes two."""
+@pytest.mark.parametrize("per_sm", [1, 2])
+def test_one_item_more_than_the_grid(per_sm):
+    """T * G = per_sm * SMs + 1 items at H = 64 (one head group).  The forward
+    launches one CTA per SM and the backward kernels two, so with per_sm = 1
+    the forward's CTA 0 takes two items, and with per_sm = 2 the backward's
+    CTA 0 takes two (items in k_bwd_dq, tokens in k_bwd_dkv)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    _check(WL.random_rows(sms + 1, 64, 1500, 520, 520, seed=4400))
+    _check(WL.random_rows(per_sm * sms + 1, 64, 1500, 520, 520, seed=4400 + per_sm))
 
 
 def test_neighbouring_items_of_very_different_lengths():
