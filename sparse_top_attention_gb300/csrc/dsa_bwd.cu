@@ -5,14 +5,16 @@
 //   k_compact   a1: valid KV rows of every token, in slot order, and counts
 //   k_bwd_dq    b1-b5: per (token, 64-head group; 32 heads when H <= 32)
 //               delta_a = rowsum(dout * out) (the FlashAttention "dpsum"
-//               preprocess, done by the softmax warps while the item's first
-//               S / dP GEMMs run), recompute P, form dS, accumulate dQ in TMEM
-//               and store dq with the exact-delta correction;
-//               write the dS' and P
-//               tiles of every 128-slot block to a bf16 scratch.  One
-//               persistent CTA per SM walks the (token, group) items.
-//   k_bwd_dkv   b6: per token, dKV_blk^T = [Q^T | dO^T] [dS'; P] over all
-//               heads at once, scatter-added into the fp32 accumulator
+//               preprocess, formed by the softmax warps one item ahead while
+//               the current item's last S / dP GEMMs run), recompute P, form
+//               dS, accumulate dQ in TMEM and store dq with the exact-delta
+//               correction; write the dS' and P tiles of every 128-slot block
+//               to a bf16 scratch.  Persistent CTAs, twice as many as SMs,
+//               walk the (token, group) items.
+//   k_bwd_dkv   b6: per token, dKV_blk^T = [Q^T | dO^T] [dS''; P] over all
+//               heads at once (dS'' = dS' - c P, the exact-delta fixup),
+//               scatter-added into the fp32 accumulator; persistent CTAs,
+//               twice as many as SMs, walk the tokens
 //   k_dkv_cast  fp32 accumulator -> bf16 dkv (k_dkv_cast_fixed for the int64
 //               fixed-point accumulator of DSA_FLAG_DETERMINISTIC)
 //   k_dsink     b7: d_sink[h] = sum_t (-p_sink * delta), fixed order
@@ -998,8 +1000,8 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // Descriptors are built once and stepped by constants (the start
-      // address field counts 16-byte units); accumulators and A stages
-      // alternate by parity.
+      // address field counts 16-byte units); the two A stages alternate by
+      // parity and the four accumulators go round in turn.
       const uint32_t id = idesc_bf16(128, kBlk, true, true);
       const uint64_t da0 = sdesc_sw128(sbase + kOffA, a_half, 1024);   // Q^T / dO^T, MN-major
       const uint64_t db0 = sdesc_sw128(sbase + kOffB, b_half, 1024);   // [dS''; P], MN-major

@@ -669,6 +669,7 @@ cudaError_t launch_fwd_hg(const Problem& p, const void* q, const void* kv, const
   const long long items = static_cast<long long>(p.T) * G;
   if (items == 0) return cudaSuccess;
   // persistent: at most one CTA per SM, each walking its share of the items
+  // (twice as many CTAs, a second wave as in the backward, is no faster here)
   const int grid = static_cast<int>(items < sm_count() ? items : sm_count());
   CUtensorMap tm_q, tm_kv;
   const int box_heads = p.H < kHG ? p.H : kHG;  // never larger than the tensor
