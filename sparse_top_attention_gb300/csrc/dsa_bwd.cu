@@ -1072,40 +1072,57 @@ k_bwd_dkv(const __grid_constant__ CUtensorMap tm_qa, const __grid_constant__ CUt
       named_bar_sync(6, kFixThreads);
       for (int b = 0; b < nblk; ++b, ++gb) {
         mbar_wait(smem_u32(&m.b_full), gb & 1, fs, 26);
-        // 16 HP pieces (a multiple of 4 x 128): four independent pieces per
-        // round, loads first, so that their latencies overlap
-        for (int p0 = ftid; p0 < 16 * HP; p0 += 4 * kFixThreads) {
+        // 16 HP pieces of 16 bytes (a multiple of kFixThreads, since HP is a
+        // multiple of 32).  Whole rounds of four independent pieces, loads
+        // first so that their latencies overlap (all of them at HP = 64 and
+        // 128), then one piece at a time for the rest (HP = 32 and 96).
+        const int npce = 16 * HP;
+        auto piece_addr = [&](int pce, float& cp) {
+          const int box = pce / (8 * HP), rem = pce - box * 8 * HP;
+          cp = m.c[rem >> 3];
+          return sbase + kOffB + box * b_half + rem * 16;
+        };
+        auto fix_piece = [&](uint32_t a, float cp, uint32_t (&dw)[4], const uint32_t (&pw)[4]) {
+          if (cp == 0.f) return;  // padded heads, or nothing to correct
+          // packed bf16 FMA, one rounding: -c (bf16) * P + dS'
+          const __nv_bfloat162 nc = __float2bfloat162_rn(-cp);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 r =
+                __hfma2(nc, *reinterpret_cast<const __nv_bfloat162*>(&pw[k]),
+                        *reinterpret_cast<const __nv_bfloat162*>(&dw[k]));
+            dw[k] = *reinterpret_cast<const uint32_t*>(&r);
+          }
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(dw[0]), "r"(dw[1]),
+                       "r"(dw[2]), "r"(dw[3])
+                       : "memory");
+        };
+        auto ld4 = [](uint32_t a, uint32_t (&w)[4]) {
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                       : "r"(a));
+        };
+        const uint32_t p_off = static_cast<uint32_t>(HP) * 128u;  // P rows after the dS' rows
+        int p0 = ftid;
+        for (; p0 + 3 * kFixThreads < npce; p0 += 4 * kFixThreads) {
           uint32_t a[4], dw[4][4], pw[4][4];
           float c[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int pce = p0 + u * kFixThreads;
-            const int box = pce / (8 * HP), rem = pce - box * 8 * HP;
-            c[u] = m.c[rem >> 3];
-            a[u] = sbase + kOffB + box * b_half + rem * 16;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(dw[u][0]), "=r"(dw[u][1]), "=r"(dw[u][2]), "=r"(dw[u][3])
-                         : "r"(a[u]));
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(pw[u][0]), "=r"(pw[u][1]), "=r"(pw[u][2]), "=r"(pw[u][3])
-                         : "r"(a[u] + static_cast<uint32_t>(HP) * 128u));
+            a[u] = piece_addr(p0 + u * kFixThreads, c[u]);
+            ld4(a[u], dw[u]);
+            ld4(a[u] + p_off, pw[u]);
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            if (c[u] == 0.f) continue;  // padded heads, or nothing to correct
-            // packed bf16 FMA, one rounding: -c (bf16) * P + dS'
-            const __nv_bfloat162 nc = __float2bfloat162_rn(-c[u]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const __nv_bfloat162 r =
-                  __hfma2(nc, *reinterpret_cast<const __nv_bfloat162*>(&pw[u][k]),
-                          *reinterpret_cast<const __nv_bfloat162*>(&dw[u][k]));
-              dw[u][k] = *reinterpret_cast<const uint32_t*>(&r);
-            }
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a[u]), "r"(dw[u][0]),
-                         "r"(dw[u][1]), "r"(dw[u][2]), "r"(dw[u][3])
-                         : "memory");
-          }
+          for (int u = 0; u < 4; ++u) fix_piece(a[u], c[u], dw[u], pw[u]);
+        }
+        for (; p0 < npce; p0 += kFixThreads) {
+          uint32_t dw[4], pw[4];
+          float c;
+          const uint32_t a = piece_addr(p0, c);
+          ld4(a, dw);
+          ld4(a + p_off, pw);
+          fix_piece(a, c, dw, pw);
         }
         fence_proxy_async_smem();  // generic-proxy writes -> the UMMA reads
         mbar_arrive(smem_u32(&m.b_fixed));
