@@ -68,20 +68,41 @@ class ClockSampler:
         self.gpu = gpu_index
         self.path = None
 
+    def _launch(self, interval_ms: int, wait_s: float) -> bool:
+        """Start nvidia-smi polling every interval_ms; True once it has
+        written a sample (the timed region must not start before that)."""
+        fd, self.path = tempfile.mkstemp(prefix="dsa_clocks_", suffix=".csv")
+        self.fh = os.fdopen(fd, "w")
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+             "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+            stdout=self.fh, stderr=subprocess.DEVNULL)
+        t0 = time.time()
+        while time.time() - t0 < wait_s and os.path.getsize(self.path) == 0:
+            time.sleep(0.01)
+        return os.path.getsize(self.path) > 0
+
     def start(self):
+        # Every 10 ms, so that a timed region of a fraction of a second still
+        # holds a dozen samples; every 50 ms if that interval yields nothing.
         try:
-            fd, self.path = tempfile.mkstemp(prefix="dsa_clocks_", suffix=".csv")
-            self.fh = os.fdopen(fd, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=self.fh, stderr=subprocess.DEVNULL)
-            # Do not start the timed region before the sampler is producing.
-            t0 = time.time()
-            while time.time() - t0 < 10.0 and os.path.getsize(self.path) == 0:
-                time.sleep(0.05)
+            if not self._launch(10, 2.0):
+                self._discard()
+                self._launch(50, 10.0)
         except Exception:
             self.proc = None
+
+    def _discard(self):
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
 
     def stop(self):
         if self.proc is None:
