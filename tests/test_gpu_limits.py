@@ -1,7 +1,8 @@
 """GPU parity at the limits of the sizes: no tokens, one token, the widest and
 narrowest index rows, a single KV row, one head, a ragged head group
-(H = 33) and a head count that leaves a single real head in the last
-64-head group of both the forward and the backward (H = 65).  The widest rows
+(H = 33), a head count that leaves a single real head in the last
+64-head group of both the forward and the backward (H = 65), and last groups
+that are partly filled (H = 48, 80, 112).  The widest rows
 also run at 16 and 24 heads, where the forward uses its 16- and 32-head
 instances, whose KV ring wraps many times within one item (16 blocks)."""
 import numpy as np
@@ -27,6 +28,12 @@ CASES = [
     ("h128", (200, 128, 900, 300, 300, False)),
     ("h16_widest_rows", (64, 16, 3000, 2048, 2048, False)),
     ("h24_widest_rows_compact", (48, 24, 3000, 2048, 2048, True)),
+    # partly filled last head groups: 48 of 64 heads; 16 and 48 real heads in
+    # the second 64-head group (padded rows of k_bwd_dq's Q/dO tiles, and
+    # k_bwd_dkv's 96- and 128-row head padding)
+    ("h48_one_partial_group", (200, 48, 900, 300, 300, False)),
+    ("h80_sixteen_heads_in_last_group", (160, 80, 900, 640, 600, True)),
+    ("h112_forty_eight_heads_in_last_group", (160, 112, 900, 640, 600, False)),
 ]
 
 
